@@ -1,0 +1,236 @@
+/*
+ * mhc_boundary.h -- C ABI of the GB300 mHC sublayer boundary library.
+ *
+ * The mHC (multi-stream hyper-connection) sublayer boundary of a
+ * DSV4.1 / GLM-style decoder, for one GPU where the tp partial sublayer
+ * outputs already sit in local HBM.  One call, in order:
+ *   1. sums the tp BF16 partials in FP32 in rank order, rounds to BF16
+ *      (or folds an unfinalised MoE output: top-k weighted routed rows plus
+ *      the shared expert, per rank, then the same rank-order sum);
+ *   2. post-mixes the hc = 4 residual streams;
+ *   3. takes the 24-way prenorm GEMV of the new streams against hc_fn and
+ *      their sum of squares;
+ *   4. derives pre (on the caller's stream) and, on a library side stream,
+ *      post and the Sinkhorn residual mix for the next boundary;
+ *   5. collapses the streams with pre and RMS-normalises the result, with an
+ *      optional MXFP8 copy (E4M3 values, UE8M0 scales per 32 elements in the
+ *      swizzled 128x4 layout).
+ *
+ * Sources (web pages, by title and the class / method on them):
+ *   [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc --
+ *         AllReduceMhcBoundary.__init__ / __call__ / join,
+ *         _BoundaryDeviceKernel.kernel, _MixesDeviceKernel._sinkhorn.
+ *   [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc --
+ *         AllReduceMHC.__call__ / finalize / _check / _consumer,
+ *         _LamportMHCDeviceKernel.kernel, _QuadFinalizePublishDeviceKernel.
+ *
+ * Conventions for every entry point:
+ *   - BF16 tensors are passed as their 16-bit patterns (void pointers).
+ *   - Unless a function says "host", pointers are DEVICE pointers on the
+ *     handle's device; the caller allocates and owns every buffer.  The
+ *     library owns only its handle, a side stream, two events and scratch
+ *     that it allocates in mhc_boundary_create (nothing is allocated later).
+ *   - Tensors are dense row-major with the shapes given below.  BF16, FP8
+ *     and hc_fn pointers must be 16-byte aligned, FP32 / int32 pointers
+ *     4-byte aligned.
+ *   - Errors: every argument is checked before the first launch; on error
+ *     the call returns a non-zero status, launches nothing and leaves the
+ *     handle's state unchanged ([DSV] AllReduceMHC._consumer: a bad argument
+ *     raises with the state untouched).  A CUDA launch failure returns
+ *     MHC_ERR_CUDA.  mhc_last_error() gives the message.  Nothing aborts,
+ *     exits or traps.
+ *   - A handle is not safe for concurrent use from several host threads.
+ */
+#ifndef MHC_BOUNDARY_H
+#define MHC_BOUNDARY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *mhc_stream_t;
+
+typedef enum {
+  MHC_OK = 0,
+  MHC_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or shape is wrong */
+  MHC_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  MHC_ERR_CAPACITY = 3,    /* m outside [1, max_num_tokens] */
+  MHC_ERR_CUDA = 4,        /* a CUDA call failed */
+  MHC_ERR_OOM = 5,         /* device allocation failed in create */
+  MHC_ERR_TIMEOUT = 6      /* reserved: no call waits on device flags */
+} mhc_status_t;
+
+/* Config flags. */
+enum {
+  /* Accept mxfp8_values / mxfp8_scales (needs hidden % 128 == 0);
+   * [DSV] AllReduceMHC(quantize_layer_input=True). */
+  MHC_FLAG_MXFP8 = 1u << 0,
+  /* Run the post / Sinkhorn kernel on the caller's stream instead of the
+   * library side stream: post_out / comb_out are then ordered like every
+   * other output and join() is a no-op. */
+  MHC_FLAG_SYNC_MIXES = 1u << 1,
+  /* Allocate device staging buffers in create so that mhc_boundary_run_host
+   * can take host pointers. */
+  MHC_FLAG_HOST_STAGING = 1u << 2
+};
+
+/* Construction arguments ([GLM] AllReduceMhcBoundary.__init__, [DSV]
+ * AllReduceMHC.__init__).  hc_mult must be 4 (the 24 mixes are
+ * 2*hc + hc*hc); hidden % 8 == 0; 1 <= tp <= 32; top_k = 0 disables
+ * finalize_moe, else 1 <= top_k <= 64. */
+typedef struct {
+  int32_t hidden;          /* H */
+  int32_t hc_mult;         /* hc, must be 4 */
+  int32_t tp;              /* number of partial sums per token */
+  int32_t max_num_tokens;  /* capacity: largest m of any call */
+  int32_t sinkhorn_repeat; /* Sinkhorn rounds, >= 1 */
+  int32_t top_k;           /* routes per token for finalize_moe (0: none) */
+  float rms_eps;           /* epsilon of the prenorm RMS */
+  float hc_eps;            /* pre-mix offset and Sinkhorn epsilon */
+  float post_mult;         /* post-mix multiplier */
+  float norm_eps;          /* RMSNorm epsilon */
+  uint32_t flags;          /* MHC_FLAG_* */
+} mhc_boundary_config_t;
+
+typedef struct mhc_boundary mhc_boundary_t; /* opaque, library-owned */
+
+/* Arguments of one boundary call over m tokens.
+ * Inputs:
+ *   partials    [tp][m][H] bf16: rank r's partial sublayer output (rank-major)
+ *   residual    [m][4][H]  bf16: the hc residual streams
+ *   post        [m][4]     f32 : post-mix of the previous boundary
+ *   comb        [m][4][4]  f32 : residual mix, indexed [source][target]
+ *   hc_fn       [4H][24]   f32 : prenorm GEMV weight, row j*H + h
+ *   scale       [3]        f32 : mix scales (pre, post, comb)
+ *   base        [24]       f32 : mix biases (pre 0..3, post 4..7, comb 8..23)
+ *   norm_weight [H]        bf16: RMSNorm weight
+ * Outputs (required):
+ *   residual_out [m][4][H] bf16: post-mixed streams
+ *   layer_input  [m][H]    bf16: RMS-normalised collapse
+ *   post_out     [m][4]    f32 : next boundary's post-mix   (side stream)
+ *   comb_out     [m][4][4] f32 : next boundary's Sinkhorn mix (side stream)
+ * Outputs (optional, NULL = not written):
+ *   pre_out      [m][4]    f32 : pre-mix used for the collapse
+ *   mixes_out    [m][24]   f32 : normalised GEMV outputs ("raw mixes")
+ *   reduced_out  [m][H]    bf16: the stage-1 sum
+ *   mxfp8_values [m][H]    u8  : E4M3 copy of layer_input   (MHC_FLAG_MXFP8)
+ *   mxfp8_scales mhc_mxfp8_scale_bytes(m, H) u8: UE8M0 scales, 128x4
+ *                swizzled, padding rows zeroed; both or neither. */
+typedef struct {
+  int32_t m;
+  const void *partials;
+  const void *residual;
+  const float *post;
+  const float *comb;
+  const float *hc_fn;
+  const float *scale;
+  const float *base;
+  const void *norm_weight;
+  void *residual_out;
+  void *layer_input;
+  float *post_out;
+  float *comb_out;
+  float *pre_out;
+  float *mixes_out;
+  void *reduced_out;
+  uint8_t *mxfp8_values;
+  uint8_t *mxfp8_scales;
+} mhc_run_args_t;
+
+/* Arguments of a boundary call whose stage 1 folds an unfinalised MoE output
+ * ([DSV] AllReduceMHC.finalize and _QuadFinalizePublishDeviceKernel; [GLM]
+ * AllReduceMhcBoundary.__call__ with a MoEOutput).  run.partials must be
+ * NULL; every other field of run is as for mhc_boundary_run.
+ *   routed  [tp][rows_per_rank][H] bf16: each rank's unweighted expert rows
+ *   idx     [tp][m][top_k] int32: row of each route in routed[r], -1 for a
+ *           route the rank does not hold; any other out-of-range value adds
+ *           nothing and is reported by mhc_boundary_check_errors
+ *   weights [m][top_k] f32: routing weights, already scaled
+ *   shared  [tp][m][H] bf16: each rank's shared-expert partial output
+ * Per rank: x_r = bf16(sum_k weights * routed_r[idx] + shared_r), the routes
+ * in k order as fused multiply-adds; then the stage-1 sum over r. */
+typedef struct {
+  mhc_run_args_t run;
+  int32_t rows_per_rank;
+  const void *routed;
+  const int32_t *idx;
+  const float *weights;
+  const void *shared;
+} mhc_moe_args_t;
+
+/* Creates a boundary on `device` (it becomes current only inside library
+ * calls).  Allocates the side stream, its events and the scratch for
+ * max_num_tokens tokens.  *out is set only on MHC_OK. */
+mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device,
+                                 mhc_boundary_t **out);
+
+/* One boundary call on `stream` ([GLM] AllReduceMhcBoundary.__call__).  It
+ * first makes `stream` wait for the previous call's side-stream kernel (the
+ * automatic join), then launches the main kernels on `stream` and the
+ * post / Sinkhorn kernel on the side stream.  post_out and comb_out are valid
+ * for `stream` only after mhc_boundary_join (or the next call). */
+mhc_status_t mhc_boundary_run(mhc_boundary_t *b, const mhc_run_args_t *args,
+                              mhc_stream_t stream);
+
+/* mhc_boundary_run with the MoE fold as stage 1 (needs top_k > 0). */
+mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *args,
+                                       mhc_stream_t stream);
+
+/* Makes `stream` wait for the last side-stream kernel ([GLM]
+ * AllReduceMhcBoundary.join).  Cheap; may be called any number of times. */
+mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream);
+
+/* mhc_boundary_run with HOST pointers in `args` (every tensor in host
+ * memory; pinned memory makes the copies asynchronous).  Needs
+ * MHC_FLAG_HOST_STAGING.  Copies the inputs to library staging buffers on
+ * `stream`, runs, joins, copies the outputs back and synchronises `stream`
+ * before returning. */
+mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *args,
+                                   mhc_stream_t stream);
+
+/* Synchronises the handle's streams and reports device-detected argument
+ * errors of earlier calls (an out-of-range MoE route index): MHC_OK or
+ * MHC_ERR_INVALID_ARG (the flag is cleared). */
+mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b);
+
+/* Waits for the side stream, frees everything the handle owns. NULL is OK. */
+mhc_status_t mhc_boundary_destroy(mhc_boundary_t *b);
+
+/* Bytes of the MXFP8 scale buffer: rows padded to a multiple of 128 times
+ * the 32-element blocks per row padded to a multiple of 4 ([DSV]
+ * mxfp8_scale_bytes). 0 if hidden % 32 != 0 or m < 1. */
+size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden);
+
+/* Device time of each kernel, summed over the calls recorded between
+ * mhc_boundary_profile_begin and mhc_boundary_profile_end (for measurement
+ * tools; off by default). */
+typedef struct {
+  int32_t calls;    /* calls recorded */
+  float stage_ms;   /* stage kernel: stage 1 / MoE fold, post-mix, partial GEMV */
+  float finish_ms;  /* finish kernel: pre, collapse, RMSNorm, MXFP8 */
+  float mixes_ms;   /* side kernel: post and Sinkhorn */
+} mhc_profile_t;
+
+/* Records CUDA events around every kernel of the next max_calls calls (events
+ * are created here, not per call).  Calls beyond max_calls are not recorded. */
+mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls);
+/* Synchronises the recorded events, writes the sums to *out and stops
+ * recording (the events are destroyed). */
+mhc_status_t mhc_boundary_profile_end(mhc_boundary_t *b, mhc_profile_t *out);
+
+/* Kernels one run / finalize_moe call launches (main stream + side stream). */
+int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b);
+
+const char *mhc_status_string(mhc_status_t status);
+/* Message of the handle's last failure ("" if none); NULL handle: the last
+ * failure of mhc_boundary_create on this thread. */
+const char *mhc_last_error(const mhc_boundary_t *b);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MHC_BOUNDARY_H */

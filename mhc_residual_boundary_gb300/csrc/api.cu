@@ -1,0 +1,532 @@
+// api.cu -- host implementation of include/mhc_boundary.h.
+//
+// Call structure ([GLM] AllReduceMhcBoundary.__call__ / join): the caller's
+// stream first waits for the previous call's side kernel; the stage kernel
+// and the finish kernel (programmatic dependent launch) run on the caller's
+// stream; an event then lets the side stream run the post / Sinkhorn kernel,
+// whose completion event the next call (or join) waits for.  Every argument
+// is validated before the first launch and a failing call leaves the handle
+// unchanged ([DSV] AllReduceMHC._consumer).
+//
+// Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
+//        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "launch.cuh"
+#include "mhc_boundary.h"
+
+using namespace mhc;
+
+struct mhc_boundary {
+  mhc_boundary_config_t cfg;
+  int device = 0;
+  int slices = 0;
+  cudaStream_t side = nullptr;
+  cudaEvent_t main_ready = nullptr;
+  cudaEvent_t side_done = nullptr;
+  bool side_pending = false;
+  float *mixes = nullptr;        // [cap][24] raw mixes read by the side kernel
+  float *part = nullptr;         // [cap][slices][25] stage-kernel partial sums
+  unsigned int *err = nullptr;   // device-detected argument errors
+  unsigned char *staging = nullptr;
+  size_t staging_bytes = 0;
+  // profiling: 6 events per recorded call (stage, finish, mixes: start/end)
+  std::vector<cudaEvent_t> prof_events;
+  int prof_capacity = 0;
+  int prof_calls = 0;
+  std::string last_error;
+};
+
+namespace {
+
+thread_local std::string g_create_error;
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int device) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != device) cudaSetDevice(device);
+  }
+  ~DeviceGuard() {
+    int now = -1;
+    if (prev >= 0 && cudaGetDevice(&now) == cudaSuccess && now != prev) cudaSetDevice(prev);
+  }
+};
+
+mhc_status_t fail(std::string &slot, mhc_status_t status, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  slot = buf;
+  return status;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t scale_bytes(int32_t m, int32_t hidden) {
+  if (m < 1 || hidden < 32 || hidden % 32) return 0;
+  return size_t((m + 127) / 128) * 128 * size_t((hidden / 32 + 3) / 4 * 4);
+}
+
+// Checks of one call; fills msg and returns non-OK on the first problem.
+mhc_status_t validate(const mhc_boundary *b, const mhc_run_args_t *a, bool moe, std::string &msg) {
+  const mhc_boundary_config_t &c = b->cfg;
+  if (!a) return fail(msg, MHC_ERR_INVALID_ARG, "args is NULL");
+  if (a->m < 1 || a->m > c.max_num_tokens)
+    return fail(msg, MHC_ERR_CAPACITY, "M=%d is outside [1, %d]", a->m, c.max_num_tokens);
+  struct Need { const void *p; const char *name; size_t align; };
+  const Need required[] = {
+      {a->residual, "residual", 16}, {a->post, "post", 4}, {a->comb, "comb", 4},
+      {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
+      {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
+      {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4},
+      {a->comb_out, "comb_out", 4}};
+  for (const Need &n : required) {
+    if (!n.p) return fail(msg, MHC_ERR_INVALID_ARG, "%s is NULL", n.name);
+    if (!aligned(n.p, n.align))
+      return fail(msg, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
+  }
+  if (moe) {
+    if (a->partials) return fail(msg, MHC_ERR_INVALID_ARG, "partials must be NULL for finalize_moe");
+  } else {
+    if (!a->partials) return fail(msg, MHC_ERR_INVALID_ARG, "partials is NULL");
+    if (!aligned(a->partials, 16)) return fail(msg, MHC_ERR_INVALID_ARG, "partials is not 16-byte aligned");
+  }
+  const Need optional[] = {{a->pre_out, "pre_out", 4}, {a->mixes_out, "mixes_out", 4},
+                           {a->reduced_out, "reduced_out", 16}, {a->mxfp8_values, "mxfp8_values", 16},
+                           {a->mxfp8_scales, "mxfp8_scales", 16}};
+  for (const Need &n : optional)
+    if (n.p && !aligned(n.p, n.align))
+      return fail(msg, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
+  if ((a->mxfp8_values == nullptr) != (a->mxfp8_scales == nullptr))
+    return fail(msg, MHC_ERR_INVALID_ARG, "mxfp8_values and mxfp8_scales are both given or both NULL");
+  if (a->mxfp8_values && !(c.flags & MHC_FLAG_MXFP8))
+    return fail(msg, MHC_ERR_UNSUPPORTED, "created without MHC_FLAG_MXFP8");
+  return MHC_OK;
+}
+
+mhc_status_t validate_moe(const mhc_boundary *b, const mhc_moe_args_t *a, std::string &msg) {
+  if (!a) return fail(msg, MHC_ERR_INVALID_ARG, "args is NULL");
+  if (b->cfg.top_k < 1) return fail(msg, MHC_ERR_UNSUPPORTED, "created with top_k = 0");
+  mhc_status_t s = validate(b, &a->run, true, msg);
+  if (s != MHC_OK) return s;
+  if (a->rows_per_rank < 1) return fail(msg, MHC_ERR_INVALID_ARG, "rows_per_rank must be >= 1");
+  if (!a->routed || !a->idx || !a->weights || !a->shared)
+    return fail(msg, MHC_ERR_INVALID_ARG, "routed, idx, weights and shared are required");
+  if (!aligned(a->routed, 16) || !aligned(a->shared, 16))
+    return fail(msg, MHC_ERR_INVALID_ARG, "routed and shared must be 16-byte aligned");
+  if (!aligned(a->idx, 4) || !aligned(a->weights, 4))
+    return fail(msg, MHC_ERR_INVALID_ARG, "idx and weights must be 4-byte aligned");
+  return MHC_OK;
+}
+
+mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe_args_t *moe,
+                         cudaStream_t stream) {
+  const mhc_boundary_config_t &c = b->cfg;
+  cudaError_t e = cudaSuccess;
+  if (b->side_pending) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+  cudaEvent_t *ev = nullptr;   // 6 events of this call when profiling
+  if (b->prof_calls < b->prof_capacity) ev = &b->prof_events[size_t(b->prof_calls) * 6];
+  const bool sync_mixes = (c.flags & MHC_FLAG_SYNC_MIXES) != 0;
+  if (ev) cudaEventRecord(ev[0], stream);
+
+  StageParams sp = {};
+  sp.m = a->m;
+  sp.hidden = c.hidden;
+  sp.tp = c.tp;
+  sp.slices = b->slices;
+  sp.partials = static_cast<const uint16_t *>(a->partials);
+  if (moe) {
+    sp.routed = static_cast<const uint16_t *>(moe->routed);
+    sp.idx = moe->idx;
+    sp.weights = moe->weights;
+    sp.shared = static_cast<const uint16_t *>(moe->shared);
+    sp.top_k = c.top_k;
+    sp.rows_per_rank = moe->rows_per_rank;
+  }
+  sp.residual = static_cast<const uint16_t *>(a->residual);
+  sp.post = a->post;
+  sp.comb = a->comb;
+  sp.hc_fn = a->hc_fn;
+  sp.residual_out = static_cast<uint16_t *>(a->residual_out);
+  sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+  sp.part = b->part;
+  sp.err = b->err;
+  e = launch_stage(sp, moe != nullptr, stream);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
+  if (ev) {
+    cudaEventRecord(ev[1], stream);
+    cudaEventRecord(ev[2], stream);
+  }
+
+  FinishParams fp = {};
+  fp.m = a->m;
+  fp.hidden = c.hidden;
+  fp.slices = b->slices;
+  fp.part = b->part;
+  fp.scale = a->scale;
+  fp.base = a->base;
+  fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
+  fp.streams = static_cast<const uint16_t *>(a->residual_out);
+  fp.rms_eps = c.rms_eps;
+  fp.hc_eps = c.hc_eps;
+  fp.norm_eps = c.norm_eps;
+  fp.mixes = b->mixes;
+  fp.mixes_out = a->mixes_out;
+  fp.pre_out = a->pre_out;
+  fp.layer_input = static_cast<uint16_t *>(a->layer_input);
+  fp.mx_values = a->mxfp8_values;
+  fp.mx_scales = a->mxfp8_scales;
+  e = launch_finish(fp, stream, ev == nullptr);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
+  if (ev) cudaEventRecord(ev[3], stream);
+
+  MixesParams mp = {};
+  mp.m = a->m;
+  mp.repeat = c.sinkhorn_repeat;
+  mp.mixes = b->mixes;
+  mp.scale = a->scale;
+  mp.base = a->base;
+  mp.post_mult = c.post_mult;
+  mp.eps = c.hc_eps;
+  mp.post_out = a->post_out;
+  mp.comb_out = a->comb_out;
+  cudaStream_t mix_stream = sync_mixes ? stream : b->side;
+  if (!sync_mixes) {
+    e = cudaEventRecord(b->main_ready, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(b->side, b->main_ready, 0);
+  }
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], mix_stream);
+  if (e == cudaSuccess) e = launch_mixes(mp, mix_stream);
+  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[5], mix_stream);
+  if (e == cudaSuccess) e = cudaEventRecord(b->side_done, mix_stream);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
+  if (ev) ++b->prof_calls;
+  b->side_pending = true;
+  b->last_error.clear();
+  return MHC_OK;
+}
+
+// Staging layout for mhc_boundary_run_host: every tensor at 256-byte offsets.
+struct Staging {
+  size_t partials, residual, post, comb, hc_fn, scale, base, gamma;
+  size_t residual_out, layer_input, post_out, comb_out, pre_out, mixes_out, reduced_out;
+  size_t mx_values, mx_scales, total;
+};
+
+Staging staging_layout(const mhc_boundary_config_t &c) {
+  const size_t cap = size_t(c.max_num_tokens), H = size_t(c.hidden);
+  Staging s = {};
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    const size_t at = off;
+    off += (bytes + 255) / 256 * 256;
+    return at;
+  };
+  s.partials = take(size_t(c.tp) * cap * H * 2);
+  s.residual = take(cap * HC * H * 2);
+  s.post = take(cap * HC * 4);
+  s.comb = take(cap * HC * HC * 4);
+  s.hc_fn = take(HC * H * MIX * 4);
+  s.scale = take(3 * 4);
+  s.base = take(MIX * 4);
+  s.gamma = take(H * 2);
+  s.residual_out = take(cap * HC * H * 2);
+  s.layer_input = take(cap * H * 2);
+  s.post_out = take(cap * HC * 4);
+  s.comb_out = take(cap * HC * HC * 4);
+  s.pre_out = take(cap * HC * 4);
+  s.mixes_out = take(cap * MIX * 4);
+  s.reduced_out = take(cap * H * 2);
+  const bool mx = (c.flags & MHC_FLAG_MXFP8) != 0;
+  s.mx_values = take(mx ? cap * H : 0);
+  s.mx_scales = take(mx ? scale_bytes(c.max_num_tokens, c.hidden) : 0);
+  s.total = off;
+  return s;
+}
+
+void destroy_profile_events(mhc_boundary *b) {
+  for (cudaEvent_t ev : b->prof_events)
+    if (ev) cudaEventDestroy(ev);
+  b->prof_events.clear();
+  b->prof_capacity = 0;
+  b->prof_calls = 0;
+}
+
+void release(mhc_boundary *b) {
+  if (b->side) cudaStreamSynchronize(b->side);
+  destroy_profile_events(b);
+  if (b->staging) cudaFree(b->staging);
+  if (b->mixes) cudaFree(b->mixes);
+  if (b->part) cudaFree(b->part);
+  if (b->err) cudaFree(b->err);
+  if (b->main_ready) cudaEventDestroy(b->main_ready);
+  if (b->side_done) cudaEventDestroy(b->side_done);
+  if (b->side) cudaStreamDestroy(b->side);
+}
+
+}  // namespace
+
+extern "C" {
+
+mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device, mhc_boundary_t **out) {
+  g_create_error.clear();
+  if (!config || !out) return fail(g_create_error, MHC_ERR_INVALID_ARG, "config and out are required");
+  const mhc_boundary_config_t &c = *config;
+  if (c.hc_mult != HC) return fail(g_create_error, MHC_ERR_UNSUPPORTED, "hc_mult must be 4 (24 mixes = 2*hc + hc*hc)");
+  if (c.hidden <= 0 || c.hidden % VEC)
+    return fail(g_create_error, MHC_ERR_INVALID_ARG, "hidden must be a positive multiple of 8");
+  if (c.hidden > MAX_HIDDEN) return fail(g_create_error, MHC_ERR_UNSUPPORTED, "hidden > %d", MAX_HIDDEN);
+  if (c.tp < 1 || c.tp > 32) return fail(g_create_error, MHC_ERR_INVALID_ARG, "tp must be in [1, 32]");
+  if (c.max_num_tokens < 1 || c.max_num_tokens > (1 << 20))
+    return fail(g_create_error, MHC_ERR_INVALID_ARG, "max_num_tokens must be in [1, 2^20]");
+  if (c.sinkhorn_repeat < 1 || c.sinkhorn_repeat > 10000)
+    return fail(g_create_error, MHC_ERR_INVALID_ARG, "sinkhorn_repeat must be in [1, 10000]");
+  if (c.top_k < 0 || c.top_k > 64) return fail(g_create_error, MHC_ERR_INVALID_ARG, "top_k must be in [0, 64]");
+  if (c.top_k > 0 && stage_smem_bytes(32, true, c.tp, c.top_k) > STAGE_SMEM_LIMIT)
+    return fail(g_create_error, MHC_ERR_UNSUPPORTED, "tp * top_k = %d route slots exceed the stage kernel's shared memory",
+                c.tp * c.top_k);
+  if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
+    return fail(g_create_error, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING))
+    return fail(g_create_error, MHC_ERR_INVALID_ARG, "unknown flag bits 0x%x", c.flags);
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count)
+    return fail(g_create_error, MHC_ERR_CUDA, "device %d is not available", device);
+
+  DeviceGuard guard(device);
+  mhc_boundary *b = new (std::nothrow) mhc_boundary();
+  if (!b) return fail(g_create_error, MHC_ERR_OOM, "host allocation failed");
+  b->cfg = c;
+  b->device = device;
+  b->slices = (c.hidden + SLICE - 1) / SLICE;
+  const size_t cap = size_t(c.max_num_tokens);
+  cudaError_t e = stage_set_attributes();
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->side, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->main_ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->side_done, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    release(b);
+    delete b;
+    return fail(g_create_error, MHC_ERR_CUDA, "create: %s", cudaGetErrorString(e));
+  }
+  e = cudaMalloc(&b->mixes, cap * MIX * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&b->part, cap * b->slices * VALUES * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&b->err, sizeof(unsigned int));
+  if (e == cudaSuccess) e = cudaMemset(b->err, 0, sizeof(unsigned int));
+  if (e == cudaSuccess && (c.flags & MHC_FLAG_HOST_STAGING)) {
+    b->staging_bytes = staging_layout(c).total;
+    e = cudaMalloc(&b->staging, b->staging_bytes);
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const mhc_status_t s = e == cudaErrorMemoryAllocation ? MHC_ERR_OOM : MHC_ERR_CUDA;
+    cudaGetLastError();
+    release(b);
+    delete b;
+    return fail(g_create_error, s, "create: %s", cudaGetErrorString(e));
+  }
+  *out = b;
+  return MHC_OK;
+}
+
+mhc_status_t mhc_boundary_run(mhc_boundary_t *b, const mhc_run_args_t *args, mhc_stream_t stream) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  std::string msg;
+  const mhc_status_t s = validate(b, args, false, msg);
+  if (s != MHC_OK) {
+    b->last_error = msg;
+    return s;
+  }
+  DeviceGuard guard(b->device);
+  return launch_call(b, args, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *args, mhc_stream_t stream) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  std::string msg;
+  const mhc_status_t s = validate_moe(b, args, msg);
+  if (s != MHC_OK) {
+    b->last_error = msg;
+    return s;
+  }
+  DeviceGuard guard(b->device);
+  return launch_call(b, &args->run, args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  if (!b->side_pending) return MHC_OK;
+  DeviceGuard guard(b->device);
+  const cudaError_t e = cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), b->side_done, 0);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+  return MHC_OK;
+}
+
+mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *host, mhc_stream_t stream_) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  if (!b->staging)
+    return fail(b->last_error, MHC_ERR_UNSUPPORTED, "created without MHC_FLAG_HOST_STAGING");
+  if (!host) return fail(b->last_error, MHC_ERR_INVALID_ARG, "args is NULL");
+  const mhc_boundary_config_t &c = b->cfg;
+  const Staging L = staging_layout(c);
+  unsigned char *base = b->staging;
+  const int m = host->m;
+  const size_t M = size_t(m), H = size_t(c.hidden);
+  // the device view of the call: staging buffers wherever the caller asked
+  mhc_run_args_t d = {};
+  d.m = m;
+  d.partials = host->partials ? base + L.partials : nullptr;
+  d.residual = host->residual ? base + L.residual : nullptr;
+  d.post = host->post ? reinterpret_cast<float *>(base + L.post) : nullptr;
+  d.comb = host->comb ? reinterpret_cast<float *>(base + L.comb) : nullptr;
+  d.hc_fn = host->hc_fn ? reinterpret_cast<float *>(base + L.hc_fn) : nullptr;
+  d.scale = host->scale ? reinterpret_cast<float *>(base + L.scale) : nullptr;
+  d.base = host->base ? reinterpret_cast<float *>(base + L.base) : nullptr;
+  d.norm_weight = host->norm_weight ? base + L.gamma : nullptr;
+  d.residual_out = host->residual_out ? base + L.residual_out : nullptr;
+  d.layer_input = host->layer_input ? base + L.layer_input : nullptr;
+  d.post_out = host->post_out ? reinterpret_cast<float *>(base + L.post_out) : nullptr;
+  d.comb_out = host->comb_out ? reinterpret_cast<float *>(base + L.comb_out) : nullptr;
+  d.pre_out = host->pre_out ? reinterpret_cast<float *>(base + L.pre_out) : nullptr;
+  d.mixes_out = host->mixes_out ? reinterpret_cast<float *>(base + L.mixes_out) : nullptr;
+  d.reduced_out = host->reduced_out ? base + L.reduced_out : nullptr;
+  d.mxfp8_values = host->mxfp8_values ? base + L.mx_values : nullptr;
+  d.mxfp8_scales = host->mxfp8_scales ? base + L.mx_scales : nullptr;
+  std::string msg;
+  mhc_status_t s = validate(b, &d, false, msg);
+  if (s != MHC_OK) {
+    b->last_error = msg;
+    return s;
+  }
+  DeviceGuard guard(b->device);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  struct Copy { void *dst; const void *src; size_t bytes; };
+  const Copy in[] = {
+      {base + L.partials, host->partials, size_t(c.tp) * M * H * 2},
+      {base + L.residual, host->residual, M * HC * H * 2},
+      {base + L.post, host->post, M * HC * 4},
+      {base + L.comb, host->comb, M * HC * HC * 4},
+      {base + L.hc_fn, host->hc_fn, size_t(HC) * H * MIX * 4},
+      {base + L.scale, host->scale, 3 * 4},
+      {base + L.base, host->base, MIX * 4},
+      {base + L.gamma, host->norm_weight, H * 2}};
+  cudaError_t e = cudaSuccess;
+  for (const Copy &x : in)
+    if (e == cudaSuccess) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "host to device copy: %s", cudaGetErrorString(e));
+  s = launch_call(b, &d, nullptr, stream);
+  if (s != MHC_OK) return s;
+  if (!(c.flags & MHC_FLAG_SYNC_MIXES)) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+  const Copy out[] = {
+      {host->residual_out, d.residual_out, M * HC * H * 2},
+      {host->layer_input, d.layer_input, M * H * 2},
+      {host->post_out, d.post_out, M * HC * 4},
+      {host->comb_out, d.comb_out, M * HC * HC * 4},
+      {host->pre_out, d.pre_out, M * HC * 4},
+      {host->mixes_out, d.mixes_out, M * MIX * 4},
+      {host->reduced_out, d.reduced_out, M * H * 2},
+      {host->mxfp8_values, d.mxfp8_values, M * H},
+      {host->mxfp8_scales, d.mxfp8_scales, scale_bytes(m, c.hidden)}};
+  for (const Copy &x : out)
+    if (e == cudaSuccess && x.dst) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "device to host copy: %s", cudaGetErrorString(e));
+  return MHC_OK;
+}
+
+mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  DeviceGuard guard(b->device);
+  unsigned int flag = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&flag, b->err, sizeof flag, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && flag) e = cudaMemset(b->err, 0, sizeof flag);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "check_errors: %s", cudaGetErrorString(e));
+  if (flag & 1u)
+    return fail(b->last_error, MHC_ERR_INVALID_ARG,
+                "a MoE route index was outside [-1, rows_per_rank); the route was skipped");
+  return MHC_OK;
+}
+
+mhc_status_t mhc_boundary_destroy(mhc_boundary_t *b) {
+  if (!b) return MHC_OK;
+  {
+    DeviceGuard guard(b->device);
+    release(b);
+  }
+  delete b;
+  return MHC_OK;
+}
+
+size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden) { return scale_bytes(m, hidden); }
+
+int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) { return b ? 3 : 0; }
+
+mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  if (max_calls < 1 || max_calls > (1 << 16))
+    return fail(b->last_error, MHC_ERR_INVALID_ARG, "max_calls must be in [1, 65536]");
+  DeviceGuard guard(b->device);
+  cudaDeviceSynchronize();
+  destroy_profile_events(b);
+  b->prof_events.assign(size_t(max_calls) * 6, nullptr);
+  for (cudaEvent_t &ev : b->prof_events) {
+    const cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) {
+      destroy_profile_events(b);
+      return fail(b->last_error, MHC_ERR_CUDA, "profile_begin: %s", cudaGetErrorString(e));
+    }
+  }
+  b->prof_capacity = max_calls;
+  b->prof_calls = 0;
+  return MHC_OK;
+}
+
+mhc_status_t mhc_boundary_profile_end(mhc_boundary_t *b, mhc_profile_t *out) {
+  if (!b || !out) return MHC_ERR_INVALID_ARG;
+  DeviceGuard guard(b->device);
+  mhc_profile_t sum = {};
+  cudaError_t e = cudaDeviceSynchronize();
+  for (int i = 0; e == cudaSuccess && i < b->prof_calls; ++i) {
+    const cudaEvent_t *ev = &b->prof_events[size_t(i) * 6];
+    float ms[3] = {0.f, 0.f, 0.f};
+    for (int k = 0; k < 3 && e == cudaSuccess; ++k) e = cudaEventElapsedTime(&ms[k], ev[2 * k], ev[2 * k + 1]);
+    sum.stage_ms += ms[0];
+    sum.finish_ms += ms[1];
+    sum.mixes_ms += ms[2];
+  }
+  sum.calls = b->prof_calls;
+  destroy_profile_events(b);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "profile_end: %s", cudaGetErrorString(e));
+  *out = sum;
+  return MHC_OK;
+}
+
+const char *mhc_status_string(mhc_status_t status) {
+  switch (status) {
+    case MHC_OK: return "ok";
+    case MHC_ERR_INVALID_ARG: return "invalid argument";
+    case MHC_ERR_UNSUPPORTED: return "unsupported";
+    case MHC_ERR_CAPACITY: return "token count outside capacity";
+    case MHC_ERR_CUDA: return "CUDA error";
+    case MHC_ERR_OOM: return "out of device memory";
+    case MHC_ERR_TIMEOUT: return "timeout";
+  }
+  return "unknown status";
+}
+
+const char *mhc_last_error(const mhc_boundary_t *b) {
+  return b ? b->last_error.c_str() : g_create_error.c_str();
+}
+
+}  // extern "C"

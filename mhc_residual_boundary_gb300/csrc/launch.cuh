@@ -1,0 +1,79 @@
+// launch.cuh -- parameter blocks and launchers of the boundary kernels
+// (internal to the library; the public surface is include/mhc_boundary.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mhc {
+
+constexpr int HC = 4;           // residual streams
+constexpr int MIX = 24;         // 2*HC + HC*HC mixes
+constexpr int VALUES = MIX + 1; // the mixes and the sum of squares
+constexpr int VEC = 8;          // BF16 values per 16-byte fragment
+
+// Hidden elements a stage CTA owns (8 fragments of 8 BF16 values).
+constexpr int SLICE = 64;
+// Dynamic shared memory the stage kernel may use (of 227 KB per CTA).
+constexpr size_t STAGE_SMEM_LIMIT = 200 * 1024;
+// Largest hidden size the finish kernel's register tiling covers.
+constexpr int MAX_HIDDEN = 16384;
+
+// Stage kernel: stage-1 sum (or MoE fold), post-mix, partial GEMV + sum of
+// squares for one (token tile, hidden slice).
+struct StageParams {
+  int m, hidden, tp, slices;
+  const uint16_t *partials;   // [tp][m][H]
+  const uint16_t *routed;     // [tp][rows][H]      (MoE)
+  const int32_t *idx;         // [tp][m][K]         (MoE)
+  const float *weights;       // [m][K]             (MoE)
+  const uint16_t *shared;     // [tp][m][H]         (MoE)
+  int top_k, rows_per_rank;   //                    (MoE)
+  const uint16_t *residual;   // [m][4][H]
+  const float *post;          // [m][4]
+  const float *comb;          // [m][4][4]
+  const float *hc_fn;         // [4H][24]
+  uint16_t *residual_out;     // [m][4][H]
+  uint16_t *reduced_out;      // [m][H] or null
+  float *part;                // [m][slices][25] partial GEMV outputs + sum of squares
+  unsigned int *err;          // device error word (bit 0: bad route index)
+};
+
+// Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm
+// and the optional MXFP8 copy.
+struct FinishParams {
+  int m, hidden, slices;
+  const float *part;
+  const float *scale;
+  const float *base;
+  const uint16_t *gamma;
+  const uint16_t *streams;    // the residual_out the stage kernel wrote
+  float rms_eps, hc_eps, norm_eps;
+  float *mixes;               // [m][24] raw mixes for the side kernel
+  float *mixes_out;           // optional copy
+  float *pre_out;             // optional
+  uint16_t *layer_input;      // [m][H]
+  uint8_t *mx_values;         // [m][H] or null
+  uint8_t *mx_scales;         // mxfp8_scale_bytes(m, H) or null
+};
+
+// Side kernel: post-mix and Sinkhorn residual mix of the next boundary.
+struct MixesParams {
+  int m, repeat;
+  const float *mixes;
+  const float *scale;
+  const float *base;
+  float post_mult, eps;
+  float *post_out;            // [m][4]
+  float *comb_out;            // [m][4][4]
+};
+
+// Token tile of the stage kernel for a call of m tokens.
+int stage_tile_tokens(int m);
+size_t stage_smem_bytes(int tile_tokens, bool moe, int tp, int top_k);
+cudaError_t stage_set_attributes();
+cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream);
+cudaError_t launch_finish(const FinishParams &p, cudaStream_t stream, bool pdl);
+cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
+
+}  // namespace mhc

@@ -1,0 +1,165 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle on the
+same seeded inputs, element by element, at every workload size and on the
+edge cases (ragged slices and token tiles, tp = 1, H = 8, zero inputs,
+MXFP8 padding rows, MoE routes a rank does not hold)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_harness import compare, oracle_outputs, run_gpu, to_device, to_numpy
+from mhc_residual_boundary_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def Boundary():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from mhc_residual_boundary_gb300 import Boundary as B
+    return B
+
+
+def check(Boundary, hidden, tp, m, *, seed=0, moe=False, top_k=0, mxfp8=False, holes=0.0,
+          capacity=None, mutate=None, **cfg):
+    inp = synth.make_inputs(hidden, tp, m, top_k=top_k, moe=moe, seed=seed, holes=holes)
+    if mutate:
+        mutate(inp)
+    p = oracle.Problem(hidden, tp, m, top_k=top_k, rows_per_rank=m * top_k if moe else 0, **cfg)
+    ref = oracle_outputs(p, inp, moe=moe, mxfp8=mxfp8)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=capacity or m, top_k=top_k, mxfp8=mxfp8, **cfg)
+    try:
+        got = run_gpu(b, inp, moe=moe, mxfp8=mxfp8)
+        b.check_errors()
+    finally:
+        b.close()
+    return compare(got, ref, inp, mxfp8=mxfp8)
+
+
+def test_tiny(Boundary):
+    check(Boundary, 5120, 4, 4)
+
+
+@pytest.mark.parametrize("m", [1, 8, 32, 64])
+def test_decode_sweep(Boundary, m):
+    check(Boundary, 5120, 8, m, seed=m)
+
+
+@pytest.mark.parametrize("m", [1 << i for i in range(10)])
+def test_glm_style(Boundary, m):
+    check(Boundary, 6144, 4, m, seed=100 + m)
+
+
+def test_moe_finalize(Boundary):
+    check(Boundary, 5120, 8, 256, moe=True, top_k=8)
+
+
+@pytest.mark.parametrize("tp,k,holes,m", [(8, 8, 0.3, 37), (1, 1, 0.0, 5), (3, 5, 0.5, 70)])
+def test_moe_routes_not_held(Boundary, tp, k, holes, m):
+    check(Boundary, 512, tp, m, moe=True, top_k=k, holes=holes, seed=tp * 10 + k)
+
+
+def test_large_mxfp8(Boundary):
+    rep = check(Boundary, 6144, 8, 4096, mxfp8=True, seed=4)
+    print("large_mxfp8 report:", rep)
+
+
+@pytest.mark.parametrize("hidden,tp,m", [(8, 1, 1), (8, 3, 9), (72, 2, 17), (520, 5, 33),
+                                         (1000, 8, 300), (128, 1, 129)])
+def test_ragged_shapes(Boundary, hidden, tp, m):
+    check(Boundary, hidden, tp, m, seed=hidden + m)
+
+
+@pytest.mark.parametrize("m", [1, 127, 129, 300])
+def test_mxfp8_padding_rows(Boundary, m):
+    check(Boundary, 256, 2, m, mxfp8=True, seed=m)
+
+
+def test_capacity_larger_than_call(Boundary):
+    check(Boundary, 1024, 4, 40, capacity=1000)
+
+
+def test_zero_and_negative_zero_inputs(Boundary):
+    def zero(inp):
+        inp["partials"][:] = 0x8000          # all -0: stage 1 must return +0
+        inp["residual"][:, :, ::3] = 0
+    check(Boundary, 256, 4, 6, mutate=zero)
+
+
+def test_other_scalars(Boundary):
+    check(Boundary, 640, 2, 20, sinkhorn_repeat=3, rms_eps=1e-3, hc_eps=0.01, post_mult=1.5,
+          norm_eps=1e-2, seed=9)
+
+
+def test_sync_mixes_flag_gives_same_bits(Boundary):
+    inp = synth.make_inputs(1024, 4, 50, seed=3)
+    outs = []
+    for sync in (False, True):
+        b = Boundary(hidden=1024, tp=4, max_num_tokens=50, sync_mixes=sync)
+        outs.append(run_gpu(b, inp))
+        b.close()
+    for name in outs[0]:
+        assert np.array_equal(outs[0][name], outs[1][name]), name
+
+
+def test_back_to_back_calls_chain_mixes(Boundary):
+    # call 2 reads call 1's post_out / comb_out on the same stream: the
+    # automatic join must order it after the side kernel
+    hidden, tp, m = 2048, 4, 64
+    inp = synth.make_inputs(hidden, tp, m, seed=5)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m)
+    dev = to_device(inp)
+    o1 = b.empty_outputs(m, extras=True)
+    b.run(dev, o1)
+    dev2 = dict(dev)
+    dev2["post"], dev2["comb"] = o1["post_out"], o1["comb_out"]
+    dev2["residual"] = o1["residual_out"]
+    o2 = b.empty_outputs(m, extras=True)
+    b.run(dev2, o2)
+    b.join()
+    torch.cuda.synchronize()
+    got1, got2 = to_numpy(o1), to_numpy(o2)
+    b.close()
+    p = oracle.Problem(hidden, tp, m)
+    ref1 = oracle.boundary(p, inp)
+    inp2 = dict(inp)
+    inp2["post"], inp2["comb"], inp2["residual"] = got1["post_out"], got1["comb_out"], got1["residual_out"]
+    ref2 = oracle.boundary(p, inp2)
+    compare(got1, ref1, inp)
+    compare(got2, ref2, inp2)
+
+
+def test_run_host_matches_run(Boundary):
+    hidden, tp, m = 1024, 4, 33
+    inp = synth.make_inputs(hidden, tp, m, seed=8)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=64, host_staging=True, mxfp8=True)
+    dev_out = run_gpu(b, inp, mxfp8=True)
+    host_in = {k: v.pin_memory() for k, v in to_device(inp, device="cpu").items()}
+    host_out = b.empty_outputs(m, extras=True, mxfp8=True, device="cpu", pin_memory=True)
+    b.run_host(host_in, host_out)
+    b.close()
+    got = to_numpy(host_out)
+    for name in dev_out:
+        assert np.array_equal(got[name], dev_out[name]), name
+
+
+def test_bad_route_index_is_reported_and_skipped(Boundary):
+    hidden, tp, m, k = 256, 2, 4, 3
+    inp = synth.make_inputs(hidden, tp, m, top_k=k, moe=True, seed=2)
+    bad = inp["idx"].copy()
+    bad[1, 2, 0] = 10_000
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, top_k=k)
+    got_inp = dict(inp)
+    got_inp["idx"] = bad
+    got = run_gpu(b, got_inp, moe=True)
+    with pytest.raises(Exception, match="route index"):
+        b.check_errors()
+    b.check_errors()            # the flag is cleared once reported
+    b.close()
+    dropped = inp["idx"].copy()
+    dropped[1, 2, 0] = -1
+    ref_inp = dict(inp)
+    ref_inp["idx"] = dropped
+    ref = oracle.boundary(oracle.Problem(hidden, tp, m, top_k=k, rows_per_rank=m * k), ref_inp, moe=True)
+    compare(got, ref, ref_inp)
