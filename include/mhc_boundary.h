@@ -205,6 +205,32 @@ mhc_status_t mhc_boundary_destroy(mhc_boundary_t *b);
  * mxfp8_scale_bytes). 0 if hidden % 32 != 0 or m < 1. */
 size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden);
 
+/* One boundary call that allocates nothing.  The pages have no counterpart
+ * of this entry point: it exists for callers that cannot allocate device
+ * memory when they need a boundary -- a framework whose caching allocator
+ * already owns the device's memory budget, code that must not trigger the
+ * implicit device synchronisation a cudaMalloc / cudaFree can cause, or a
+ * thread that may not create a handle (mhc_boundary_create allocates scratch,
+ * a stream and events).  It needs no handle: `config` is read as for
+ * mhc_boundary_create (top_k is ignored; flags may hold MHC_FLAG_MXFP8 and
+ * MHC_FLAG_SYNC_MIXES) and `args` as for mhc_boundary_run, device pointers
+ * the caller allocated and owns.  All three kernels run on `stream` in order,
+ * so post_out / comb_out need no join.
+ * Scratch: an 8 MiB array of this library's device memory, which every GPU
+ * that loads the library holds until the process exits; a call needs
+ * m * (25 * ceil(H / 64) + 24) * 4 + 256 bytes of it (H = 6144: up to 865 tokens),
+ * and a larger m returns MHC_ERR_CAPACITY with nothing launched.  Every call
+ * on a device shares that array and it keeps the last call's contents
+ * (nothing needs clearing: each call writes every word it reads before
+ * reading it), so calls whose kernels overlap on the GPU race: order them on
+ * one stream or with events.  The first call on a device looks up the
+ * array's device address and sets a kernel attribute there; make that first
+ * call before any stream capture.  Runs on the current device.  On failure
+ * the message is written to error[0 .. error_len-1] (error may be NULL) and
+ * nothing is launched. */
+mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *config, const mhc_run_args_t *args,
+                                     mhc_stream_t stream, char *error, size_t error_len);
+
 /* Device time of each kernel, summed over the calls recorded between
  * mhc_boundary_profile_begin and mhc_boundary_profile_end (for measurement
  * tools; off by default). */

@@ -81,6 +81,10 @@ def lib() -> ctypes.CDLL:
                      "mhc_boundary_finalize_moe", "mhc_boundary_join", "mhc_boundary_check_errors",
                      "mhc_boundary_destroy", "mhc_boundary_profile_begin", "mhc_boundary_profile_end"):
             getattr(h, name).restype = st
+        h.mhc_boundary_run_static.argtypes = [ctypes.POINTER(mhc_boundary_config_t),
+                                               ctypes.POINTER(mhc_run_args_t), vp, ctypes.c_char_p,
+                                               ctypes.c_size_t]
+        h.mhc_boundary_run_static.restype = st
         h.mhc_mxfp8_scale_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
         h.mhc_mxfp8_scale_bytes.restype = ctypes.c_size_t
         h.mhc_boundary_launches_per_call.argtypes = [vp]
@@ -135,6 +139,16 @@ def mhc_boundary_check_errors(handle) -> None:
 
 def mhc_boundary_destroy(handle) -> None:
     _check(lib().mhc_boundary_destroy(handle), None)
+
+
+def mhc_boundary_run_static(config: mhc_boundary_config_t, args: mhc_run_args_t, stream=None) -> None:
+    """The allocation-free call: no handle, scratch in the library's static
+    device array (see include/mhc_boundary.h)."""
+    err = ctypes.create_string_buffer(512)
+    status = lib().mhc_boundary_run_static(ctypes.byref(config), ctypes.byref(args), _stream_ptr(stream),
+                                           err, len(err))
+    if status != MHC_OK:
+        raise MhcError(status, err.value.decode())
 
 
 def mhc_boundary_profile_begin(handle, max_calls: int) -> None:

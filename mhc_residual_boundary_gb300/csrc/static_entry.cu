@@ -1,0 +1,190 @@
+// static_entry.cu -- mhc_boundary_run_static: one boundary call that
+// allocates nothing.
+//
+// Some callers cannot allocate device memory when they need a boundary: a
+// framework whose caching allocator already owns the device memory budget,
+// code that must not trigger the implicit device synchronisation a
+// cudaMalloc / cudaFree can cause, or a host thread that may not create a
+// handle (mhc_boundary_create allocates its scratch, a side stream and
+// events).  This entry point runs the same three kernels as
+// mhc_boundary_run, all on the caller's stream, with their scratch (the
+// per-slice GEMV partial sums and the raw mixes) in a fixed-size array of
+// this library's device memory instead of memory the handle allocated.
+//
+// The array is a file-scope __device__ variable: every GPU that loads this
+// library holds STATIC_SCRATCH_BYTES of it until the process exits.  In host
+// code its name is only a host-side stand-in, never a device address, so the
+// host asks the runtime for the device address (cudaGetSymbolAddress) once
+// per device, with that device current, and passes that pointer to the
+// kernels.
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "launch.cuh"
+#include "mhc_boundary.h"
+
+using namespace mhc;
+
+namespace {
+
+// Scratch of every call: [m][slices][25] partial sums, then [m][24] mixes.
+constexpr size_t STATIC_SCRATCH_BYTES = size_t(8) << 20;   // 8 MiB per device
+__device__ __align__(256) float g_scratch[STATIC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_setup_mutex;
+std::atomic<float *> g_scratch_ptr[MAX_DEVICES];
+
+mhc_status_t report(char *error, size_t error_len, mhc_status_t status, const char *fmt, ...) {
+  if (error && error_len) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(error, error_len, fmt, ap);
+    va_end(ap);
+  }
+  return status;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device address of g_scratch on the current device, looked up once per
+// device; the first call on a device also raises the stage kernel's shared
+// memory limit there.
+mhc_status_t scratch_on_device(int device, float **out, char *error, size_t error_len) {
+  if (device < 0 || device >= MAX_DEVICES)
+    return report(error, error_len, MHC_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported",
+                  device, MAX_DEVICES);
+  float *ptr = g_scratch_ptr[device].load(std::memory_order_acquire);
+  if (!ptr) {
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    ptr = g_scratch_ptr[device].load(std::memory_order_relaxed);
+    if (!ptr) {
+      void *addr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&addr, g_scratch);
+      if (e == cudaSuccess) e = stage_set_attributes();
+      if (e != cudaSuccess)
+        return report(error, error_len, MHC_ERR_CUDA, "set-up on device %d: %s", device, cudaGetErrorString(e));
+      ptr = static_cast<float *>(addr);
+      g_scratch_ptr[device].store(ptr, std::memory_order_release);
+    }
+  }
+  *out = ptr;
+  return MHC_OK;
+}
+
+}  // namespace
+
+extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *config, const mhc_run_args_t *a,
+                                                mhc_stream_t stream_, char *error, size_t error_len) {
+  if (error && error_len) error[0] = '\0';
+  if (!config || !a) return report(error, error_len, MHC_ERR_INVALID_ARG, "config and args are required");
+  const mhc_boundary_config_t &c = *config;
+  if (c.hc_mult != HC) return report(error, error_len, MHC_ERR_UNSUPPORTED, "hc_mult must be 4");
+  if (c.hidden <= 0 || c.hidden % VEC)
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "hidden must be a positive multiple of 8");
+  if (c.hidden > MAX_HIDDEN) return report(error, error_len, MHC_ERR_UNSUPPORTED, "hidden > %d", MAX_HIDDEN);
+  if (c.tp < 1 || c.tp > 32) return report(error, error_len, MHC_ERR_INVALID_ARG, "tp must be in [1, 32]");
+  if (c.sinkhorn_repeat < 1 || c.sinkhorn_repeat > 10000)
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "sinkhorn_repeat must be in [1, 10000]");
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES))
+    return report(error, error_len, MHC_ERR_UNSUPPORTED, "only MHC_FLAG_MXFP8 and MHC_FLAG_SYNC_MIXES apply");
+  if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
+
+  const int slices = (c.hidden + SLICE - 1) / SLICE;
+  const size_t per_token = size_t(slices) * VALUES + MIX;    // floats
+  // the mixes start at a 64-float boundary after the partial sums
+  const size_t max_m = (STATIC_SCRATCH_BYTES / sizeof(float) - 64) / per_token;
+  if (a->m < 1 || size_t(a->m) > max_m)
+    return report(error, error_len, MHC_ERR_CAPACITY,
+                  "M=%d is outside [1, %zu]: the static scratch (%zu bytes) holds %zu floats per token at hidden=%d",
+                  a->m, max_m, STATIC_SCRATCH_BYTES, per_token, c.hidden);
+  struct Need { const void *p; const char *name; size_t align; };
+  const Need required[] = {
+      {a->partials, "partials", 16}, {a->residual, "residual", 16}, {a->post, "post", 4},
+      {a->comb, "comb", 4}, {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
+      {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
+      {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4}, {a->comb_out, "comb_out", 4}};
+  for (const Need &n : required) {
+    if (!n.p) return report(error, error_len, MHC_ERR_INVALID_ARG, "%s is NULL", n.name);
+    if (!aligned(n.p, n.align))
+      return report(error, error_len, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
+  }
+  const Need optional[] = {{a->pre_out, "pre_out", 4}, {a->mixes_out, "mixes_out", 4},
+                           {a->reduced_out, "reduced_out", 16}, {a->mxfp8_values, "mxfp8_values", 16},
+                           {a->mxfp8_scales, "mxfp8_scales", 16}};
+  for (const Need &n : optional)
+    if (n.p && !aligned(n.p, n.align))
+      return report(error, error_len, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
+  if ((a->mxfp8_values == nullptr) != (a->mxfp8_scales == nullptr))
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "mxfp8_values and mxfp8_scales go together");
+  if (a->mxfp8_values && !(c.flags & MHC_FLAG_MXFP8))
+    return report(error, error_len, MHC_ERR_UNSUPPORTED, "MXFP8 outputs need MHC_FLAG_MXFP8");
+
+  int device = -1;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  float *scratch = nullptr;
+  const mhc_status_t s = scratch_on_device(device, &scratch, error, error_len);
+  if (s != MHC_OK) return s;
+  // every scratch word a kernel reads was written earlier in the same call,
+  // so nothing needs clearing between calls
+  float *part = scratch;
+  float *mixes = scratch + (size_t(a->m) * slices * VALUES + 63) / 64 * 64;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  StageParams sp = {};
+  sp.m = a->m;
+  sp.hidden = c.hidden;
+  sp.tp = c.tp;
+  sp.slices = slices;
+  sp.partials = static_cast<const uint16_t *>(a->partials);
+  sp.residual = static_cast<const uint16_t *>(a->residual);
+  sp.post = a->post;
+  sp.comb = a->comb;
+  sp.hc_fn = a->hc_fn;
+  sp.residual_out = static_cast<uint16_t *>(a->residual_out);
+  sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+  sp.part = part;
+  sp.err = nullptr;   // read only by the MoE variant, which this entry point does not run
+  e = launch_stage(sp, false, stream);
+  if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
+
+  FinishParams fp = {};
+  fp.m = a->m;
+  fp.hidden = c.hidden;
+  fp.slices = slices;
+  fp.part = part;
+  fp.scale = a->scale;
+  fp.base = a->base;
+  fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
+  fp.streams = static_cast<const uint16_t *>(a->residual_out);
+  fp.rms_eps = c.rms_eps;
+  fp.hc_eps = c.hc_eps;
+  fp.norm_eps = c.norm_eps;
+  fp.mixes = mixes;
+  fp.mixes_out = a->mixes_out;
+  fp.pre_out = a->pre_out;
+  fp.layer_input = static_cast<uint16_t *>(a->layer_input);
+  fp.mx_values = a->mxfp8_values;
+  fp.mx_scales = a->mxfp8_scales;
+  e = launch_finish(fp, stream, true);
+  if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
+
+  MixesParams mp = {};
+  mp.m = a->m;
+  mp.repeat = c.sinkhorn_repeat;
+  mp.mixes = mixes;
+  mp.scale = a->scale;
+  mp.base = a->base;
+  mp.post_mult = c.post_mult;
+  mp.eps = c.hc_eps;
+  mp.post_out = a->post_out;
+  mp.comb_out = a->comb_out;
+  e = launch_mixes(mp, stream);
+  if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
+  return MHC_OK;
+}

@@ -1,0 +1,78 @@
+"""mhc_boundary_run_static: the allocation-free entry point.
+
+It serves callers that cannot allocate device memory when they need a
+boundary (a caching allocator that owns the device budget, code that must
+not risk the synchronisation of a cudaMalloc, threads that may not create a
+handle).  Its outputs must match the handle-based entry point's on the same
+inputs, within the parity tolerances, on two calls in a row (the second call
+reuses the static scratch the first one left behind).  The file sorts last so
+that a run stopping at its first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import to_device, to_numpy
+from mhc_residual_boundary_gb300 import synth
+from tolerances import close_f32, layer_input_ok, ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+
+def _args(capi, dev_in, outs, m):
+    a = capi.mhc_run_args_t()
+    a.m = m
+    for n in ("partials", "residual", "post", "comb", "hc_fn", "scale", "base", "norm_weight"):
+        setattr(a, n, dev_in[n].data_ptr())
+    for n, t in outs.items():
+        setattr(a, n, t.data_ptr())
+    return a
+
+
+def _same(static, handle, inputs):
+    assert np.array_equal(static["reduced_out"], handle["reduced_out"])
+    assert ulp_diff(static["residual_out"], handle["residual_out"]).max() <= 2
+    assert layer_input_ok(static["layer_input"], handle["layer_input"], handle["residual_out"],
+                          handle["pre_out"], inputs["gamma"]).all()
+    for n, atol in (("pre_out", 1e-6), ("post_out", 1e-6), ("comb_out", 1e-6), ("mixes_out", 1e-5)):
+        assert close_f32(static[n], handle[n], 1e-4, atol).all(), n
+    if "mxfp8_values" in handle:
+        assert np.array_equal(static["mxfp8_values"], handle["mxfp8_values"])
+        assert np.array_equal(static["mxfp8_scales"], handle["mxfp8_scales"])
+
+
+@pytest.mark.parametrize("hidden,tp,m,mxfp8", [(6144, 4, 256, True), (5120, 8, 37, False)])
+def test_static_entry_matches_handle_entry_twice(hidden, tp, m, mxfp8):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from mhc_residual_boundary_gb300 import Boundary, capi
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, mxfp8=mxfp8)
+    cfg = capi.mhc_boundary_config_t(hidden, 4, tp, m, 20, 0, 1e-6, 1e-6, 2.0, 1e-6,
+                                     capi.MHC_FLAG_MXFP8 if mxfp8 else 0)
+    try:
+        for seed in (11, 12):                      # two calls in a row
+            inputs = synth.make_inputs(hidden, tp, m, seed=seed)
+            dev_in = to_device(inputs)
+            ref = b.empty_outputs(m, extras=True, mxfp8=mxfp8)
+            b.run(dev_in, ref)
+            b.join()
+            got = b.empty_outputs(m, extras=True, mxfp8=mxfp8)
+            for t in got.values():
+                t.view(torch.uint8).fill_(0x5A)
+            capi.mhc_boundary_run_static(cfg, _args(capi, dev_in, got, m))
+            torch.cuda.synchronize()
+            _same(to_numpy(got), to_numpy(ref), inputs)
+    finally:
+        b.close()
+
+
+def test_static_entry_rejects_too_many_tokens():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from mhc_residual_boundary_gb300 import capi
+    hidden, tp, m = 6144, 4, 866                    # one token beyond the 8 MiB scratch
+    cfg = capi.mhc_boundary_config_t(hidden, 4, tp, m, 20, 0, 1e-6, 1e-6, 2.0, 1e-6, 0)
+    a = capi.mhc_run_args_t()
+    a.m = m
+    with pytest.raises(capi.MhcError, match="CAPACITY"):
+        capi.mhc_boundary_run_static(cfg, a)
