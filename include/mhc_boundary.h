@@ -61,7 +61,7 @@ typedef enum {
   MHC_ERR_CAPACITY = 3,    /* m outside [1, max_num_tokens] */
   MHC_ERR_CUDA = 4,        /* a CUDA call failed */
   MHC_ERR_OOM = 5,         /* device allocation failed in create */
-  MHC_ERR_TIMEOUT = 6      /* reserved: no call waits on device flags */
+  MHC_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (see check_errors) */
 } mhc_status_t;
 
 /* Config flags. */
@@ -192,9 +192,10 @@ mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream);
 mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *args,
                                    mhc_stream_t stream);
 
-/* Synchronises the handle's streams and reports device-detected argument
- * errors of earlier calls (an out-of-range MoE route index): MHC_OK or
- * MHC_ERR_INVALID_ARG (the flag is cleared). */
+/* Synchronises the handle's streams and reports device-detected errors of
+ * earlier calls: MHC_ERR_TIMEOUT if a stage kernel gave up its bounded wait
+ * for tensor-core work (its outputs are then invalid), MHC_ERR_INVALID_ARG
+ * for an out-of-range MoE route index, else MHC_OK (the flags are cleared). */
 mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b);
 
 /* Waits for the side stream, frees everything the handle owns. NULL is OK. */

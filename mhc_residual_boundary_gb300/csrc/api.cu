@@ -27,6 +27,7 @@ struct mhc_boundary {
   mhc_boundary_config_t cfg;
   int device = 0;
   int slices = 0;
+  int sm_count = 0;
   cudaStream_t side = nullptr;
   cudaEvent_t main_ready = nullptr;
   cudaEvent_t side_done = nullptr;
@@ -161,7 +162,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = b->part;
   sp.err = b->err;
-  e = launch_stage(sp, moe != nullptr, stream);
+  e = moe ? launch_stage(sp, true, stream) : launch_stage_tc(sp, b->sm_count, stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
   if (ev) {
     cudaEventRecord(ev[1], stream);
@@ -311,6 +312,8 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   b->slices = (c.hidden + SLICE - 1) / SLICE;
   const size_t cap = size_t(c.max_num_tokens);
   cudaError_t e = stage_set_attributes();
+  if (e == cudaSuccess) e = stage_tc_set_attributes();
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b->sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->main_ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->side_done, cudaEventDisableTiming);
@@ -452,6 +455,9 @@ mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b) {
   if (e == cudaSuccess) e = cudaMemcpy(&flag, b->err, sizeof flag, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && flag) e = cudaMemset(b->err, 0, sizeof flag);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "check_errors: %s", cudaGetErrorString(e));
+  if (flag & 2u)
+    return fail(b->last_error, MHC_ERR_TIMEOUT,
+                "a stage kernel gave up waiting for its tensor-core work; its outputs are not valid");
   if (flag & 1u)
     return fail(b->last_error, MHC_ERR_INVALID_ARG,
                 "a MoE route index was outside [-1, rows_per_rank); the route was skipped");

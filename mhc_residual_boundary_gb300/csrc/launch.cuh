@@ -36,7 +36,8 @@ struct StageParams {
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][slices][25] partial GEMV outputs + sum of squares
-  unsigned int *err;          // device error word (bit 0: bad route index)
+  unsigned int *err;          // device error word (bit 0: bad route index,
+                              // bit 1: a tensor-core completion wait gave up)
 };
 
 // Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm
@@ -73,6 +74,11 @@ int stage_tile_tokens(int m);
 size_t stage_smem_bytes(int tile_tokens, bool moe, int tp, int top_k);
 cudaError_t stage_set_attributes();
 cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream);
+// Stage kernel with the GEMV on tcgen05 tensor cores (non-MoE calls):
+// persistent, at most `ctas` CTAs of one per SM.
+size_t stage_tc_smem_bytes();
+cudaError_t stage_tc_set_attributes();
+cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_finish(const FinishParams &p, cudaStream_t stream, bool pdl);
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
 

@@ -37,6 +37,7 @@ __device__ __align__(256) float g_scratch[STATIC_SCRATCH_BYTES / sizeof(float)];
 constexpr int MAX_DEVICES = 64;
 std::mutex g_setup_mutex;
 std::atomic<float *> g_scratch_ptr[MAX_DEVICES];
+int g_sm_count[MAX_DEVICES];
 
 mhc_status_t report(char *error, size_t error_len, mhc_status_t status, const char *fmt, ...) {
   if (error && error_len) {
@@ -51,8 +52,8 @@ mhc_status_t report(char *error, size_t error_len, mhc_status_t status, const ch
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Device address of g_scratch on the current device, looked up once per
-// device; the first call on a device also raises the stage kernel's shared
-// memory limit there.
+// device; the first call on a device also raises the stage kernels' shared
+// memory limits there and reads its SM count.
 mhc_status_t scratch_on_device(int device, float **out, char *error, size_t error_len) {
   if (device < 0 || device >= MAX_DEVICES)
     return report(error, error_len, MHC_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported",
@@ -65,6 +66,8 @@ mhc_status_t scratch_on_device(int device, float **out, char *error, size_t erro
       void *addr = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&addr, g_scratch);
       if (e == cudaSuccess) e = stage_set_attributes();
+      if (e == cudaSuccess) e = stage_tc_set_attributes();
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sm_count[device], cudaDevAttrMultiProcessorCount, device);
       if (e != cudaSuccess)
         return report(error, error_len, MHC_ERR_CUDA, "set-up on device %d: %s", device, cudaGetErrorString(e));
       ptr = static_cast<float *>(addr);
@@ -150,7 +153,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;
   sp.err = nullptr;   // read only by the MoE variant, which this entry point does not run
-  e = launch_stage(sp, false, stream);
+  e = launch_stage_tc(sp, g_sm_count[device], stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
 
   FinishParams fp = {};
