@@ -314,6 +314,7 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         barrier(dist)
         prof = b.profile_end()
+    b.check_errors()   # a device-side timeout or bad argument fails the run here
     clock = clocks.summary()
     elapsed_ms = max_over_ranks(dist, start.elapsed_time(stop))
     value = world * w.m * args.steps / (elapsed_ms / 1e3)

@@ -30,9 +30,10 @@
  *     handle's device; the caller allocates and owns every buffer.  The
  *     library owns only its handle, a side stream, two events and scratch
  *     that it allocates in mhc_boundary_create (nothing is allocated later).
- *   - Tensors are dense row-major with the shapes given below.  BF16, FP8
- *     and hc_fn pointers must be 16-byte aligned, FP32 / int32 pointers
- *     4-byte aligned.
+ *   - Tensors are dense row-major with the shapes given below.  BF16, FP8,
+ *     hc_fn, post and comb pointers must be 16-byte aligned (the kernels move
+ *     them with 16-byte vector loads and TMA tensor copies), the other FP32 /
+ *     int32 pointers 4-byte aligned.
  *   - Errors: every argument is checked before the first launch; on error
  *     the call returns a non-zero status, launches nothing and leaves the
  *     handle's state unchanged ([DSV] AllReduceMHC._consumer: a bad argument

@@ -85,7 +85,7 @@ mhc_status_t validate(const mhc_boundary *b, const mhc_run_args_t *a, bool moe, 
     return fail(msg, MHC_ERR_CAPACITY, "M=%d is outside [1, %d]", a->m, c.max_num_tokens);
   struct Need { const void *p; const char *name; size_t align; };
   const Need required[] = {
-      {a->residual, "residual", 16}, {a->post, "post", 4}, {a->comb, "comb", 4},
+      {a->residual, "residual", 16}, {a->post, "post", 16}, {a->comb, "comb", 16},
       {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
       {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
       {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4},
@@ -144,7 +144,10 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.m = a->m;
   sp.hidden = c.hidden;
   sp.tp = c.tp;
-  sp.slices = b->slices;
+  // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
+  // groups (tensor-core kernel); the scratch holds the larger count
+  const bool tc_path = moe == nullptr && c.tp <= TP_TMA_MAX;
+  sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
   sp.partials = static_cast<const uint16_t *>(a->partials);
   if (moe) {
     sp.routed = static_cast<const uint16_t *>(moe->routed);
@@ -162,7 +165,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = b->part;
   sp.err = b->err;
-  e = moe ? launch_stage(sp, true, stream) : launch_stage_tc(sp, b->sm_count, stream);
+  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, moe != nullptr, stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
   if (ev) {
     cudaEventRecord(ev[1], stream);
@@ -172,7 +175,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   FinishParams fp = {};
   fp.m = a->m;
   fp.hidden = c.hidden;
-  fp.slices = b->slices;
+  fp.slices = sp.slices;
   fp.part = b->part;
   fp.scale = a->scale;
   fp.base = a->base;

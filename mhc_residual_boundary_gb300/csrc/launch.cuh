@@ -12,8 +12,13 @@ constexpr int MIX = 24;         // 2*HC + HC*HC mixes
 constexpr int VALUES = MIX + 1; // the mixes and the sum of squares
 constexpr int VEC = 8;          // BF16 values per 16-byte fragment
 
-// Hidden elements a stage CTA owns (8 fragments of 8 BF16 values).
+// Hidden elements a CUDA-core stage CTA owns (8 fragments of 8 BF16 values).
 constexpr int SLICE = 64;
+// Hidden columns of one tensor-core stage unit (256-byte rows).
+constexpr int TC_GROUP_COLS = 128;
+// Ranks one TMA box of the tensor-core stage kernel covers; calls with more
+// partials run the CUDA-core stage kernel.
+constexpr int TP_TMA_MAX = 8;
 // Dynamic shared memory the stage kernel may use (of 227 KB per CTA).
 constexpr size_t STAGE_SMEM_LIMIT = 200 * 1024;
 // Largest hidden size the finish kernel's register tiling covers.

@@ -107,8 +107,8 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
                   a->m, max_m, STATIC_SCRATCH_BYTES, per_token, c.hidden);
   struct Need { const void *p; const char *name; size_t align; };
   const Need required[] = {
-      {a->partials, "partials", 16}, {a->residual, "residual", 16}, {a->post, "post", 4},
-      {a->comb, "comb", 4}, {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
+      {a->partials, "partials", 16}, {a->residual, "residual", 16}, {a->post, "post", 16},
+      {a->comb, "comb", 16}, {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
       {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
       {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4}, {a->comb_out, "comb_out", 4}};
   for (const Need &n : required) {
@@ -136,14 +136,18 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   // every scratch word a kernel reads was written earlier in the same call,
   // so nothing needs clearing between calls
   float *part = scratch;
-  float *mixes = scratch + (size_t(a->m) * slices * VALUES + 63) / 64 * 64;
+  // the tensor-core stage kernel writes one partial group per 128 columns,
+  // the CUDA-core one per 64; the capacity rule above counts the latter
+  const bool tc_path = c.tp <= TP_TMA_MAX;
+  const int groups = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : slices;
+  float *mixes = scratch + (size_t(a->m) * groups * VALUES + 63) / 64 * 64;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
   StageParams sp = {};
   sp.m = a->m;
   sp.hidden = c.hidden;
   sp.tp = c.tp;
-  sp.slices = slices;
+  sp.slices = groups;
   sp.partials = static_cast<const uint16_t *>(a->partials);
   sp.residual = static_cast<const uint16_t *>(a->residual);
   sp.post = a->post;
@@ -153,13 +157,13 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;
   sp.err = nullptr;   // read only by the MoE variant, which this entry point does not run
-  e = launch_stage_tc(sp, g_sm_count[device], stream);
+  e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream) : launch_stage(sp, false, stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
 
   FinishParams fp = {};
   fp.m = a->m;
   fp.hidden = c.hidden;
-  fp.slices = slices;
+  fp.slices = groups;
   fp.part = part;
   fp.scale = a->scale;
   fp.base = a->base;

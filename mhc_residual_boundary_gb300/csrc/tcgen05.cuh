@@ -1,8 +1,8 @@
 // tcgen05.cuh -- thin inline-PTX wrappers for the 5th-generation tensor
-// cores of sm_100-class GPUs (tcgen05.*), mbarriers and proxy fences, as the
-// stage kernel uses them: one CTA, cta_group::1, BF16 x BF16 -> FP32 MMAs
-// with both operands in shared memory (no swizzle, K-major) and the
-// accumulator in tensor memory.
+// cores of sm_100-class GPUs (tcgen05.*), TMA tensor copies, mbarriers and
+// proxy fences, as the stage kernel uses them: one CTA, cta_group::1,
+// BF16 x BF16 -> FP32 MMAs with both operands in shared memory (no swizzle,
+// K-major) and the accumulator in tensor memory.
 #pragma once
 
 #include <cstdint>
@@ -42,6 +42,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (i > 64) __nanosleep(64);
   }
   return false;
+}
+
+// Adds `bytes` to the transaction count the current phase waits for and
+// arrives once (the producer's arrival).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// --------------------------------------------------------------------- TMA
+// Tiled bulk tensor copies global -> shared memory; completion is counted in
+// bytes on the mbarrier.  Coordinates are element indices, innermost first.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
 // ------------------------------------------------------------------ fences
@@ -86,6 +115,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor, no swizzle: start address, leading-
 // dimension byte offset (between core matrices adjacent along K), stride-
@@ -97,7 +138,7 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // Instruction descriptor of kind::f16: FP32 accumulator, BF16 A and B, both
 // K-major, M x N.
-constexpr uint32_t idesc_bf16_f32(int m, int n) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 

@@ -52,6 +52,7 @@ def _untouched(outs):
     ("m0", "MHC_ERR_CAPACITY"), ("m_big", "MHC_ERR_CAPACITY"), ("null_residual", "MHC_ERR_INVALID_ARG"),
     ("null_partials", "MHC_ERR_INVALID_ARG"), ("misaligned_partials", "MHC_ERR_INVALID_ARG"),
     ("misaligned_layer_input", "MHC_ERR_INVALID_ARG"), ("mxfp8_without_flag", "MHC_ERR_UNSUPPORTED"),
+    ("misaligned_post", "MHC_ERR_INVALID_ARG"),
 ])
 def test_bad_arguments_launch_nothing(env, case, status):
     b, inp, capi = env
@@ -68,6 +69,8 @@ def test_bad_arguments_launch_nothing(env, case, status):
         a.partials = None
     elif case == "misaligned_partials":
         a.partials = inp["partials"].data_ptr() + 2
+    elif case == "misaligned_post":
+        a.post = inp["post"].data_ptr() + 4
     elif case == "misaligned_layer_input":
         a.layer_input = outs["layer_input"].data_ptr() + 8
     elif case == "mxfp8_without_flag":
