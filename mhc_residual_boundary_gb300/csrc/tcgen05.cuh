@@ -127,6 +127,20 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 4 consecutive 32-bit columns of this thread's TMEM lane, without waiting.
+// The registers are valid only after tmem_wait_ld(); pass them through
+// tmem_hold4() after the wait so that no use is scheduled before it.
+__device__ __forceinline__ void tmem_ld4_async(uint32_t taddr, uint32_t *r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_hold4(uint32_t *r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
+}
+
 // ------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor, no swizzle: start address, leading-
 // dimension byte offset (between core matrices adjacent along K), stride-
