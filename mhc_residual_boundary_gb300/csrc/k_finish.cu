@@ -24,6 +24,7 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int MAXF = MAX_HIDDEN / VEC / NT;   // fragments per thread at most
+static_assert(MAXF == 8, "launch_finish dispatches NF = 1 .. 8");
 
 __device__ __forceinline__ float sigmoid(float z) {
   return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
@@ -58,7 +59,10 @@ __device__ __forceinline__ size_t swizzle_128x4(int row, int col, int cols) {
   return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (col % 4);
 }
 
+// NF: 16-byte fragments of a stream row per thread (ceil(H / 8 / 256)).
+template <int NF>
 __global__ void __launch_bounds__(NT) k_finish(const FinishParams p) {
+  extern __shared__ float part_s[];   // [slices][25] of this token
   __shared__ float tot_s[VALUES];
   __shared__ float pre_s[HC];
   __shared__ float red_s[NT / 32];
@@ -71,10 +75,26 @@ __global__ void __launch_bounds__(NT) k_finish(const FinishParams p) {
   // Nothing below may read the stage kernel's outputs before this point.
   pdl_wait();
 
+  // the token's new streams go to registers first, so that their latency
+  // overlaps the partial-sum reduction
+  uint4 sv[NF][HC];
+#pragma unroll
+  for (int i = 0; i < NF; ++i) {
+    const int fr = tid + i * NT;
+#pragma unroll
+    for (int j = 0; j < HC; ++j)
+      sv[i][j] = fr < nfrag ? ld_stream(p.streams + ((size_t)t * HC + j) * H + (size_t)fr * VEC)
+                            : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int np = p.slices * VALUES;
+  const float *prow = p.part + (size_t)t * np;
+  for (int e = tid; e < np; e += NT) part_s[e] = prow[e];
+  __syncthreads();
+
   // 1. partial sums over the slices, in slice order within each lane
   for (int v = warp; v < VALUES; v += NT / 32) {
     float s = 0.f;
-    for (int sl = lane; sl < p.slices; sl += 32) s += p.part[((size_t)t * p.slices + sl) * VALUES + v];
+    for (int sl = lane; sl < p.slices; sl += 32) s += part_s[sl * VALUES + v];
     s = warp_sum(s);
     if (lane == 0) tot_s[v] = s;
   }
@@ -98,27 +118,22 @@ __global__ void __launch_bounds__(NT) k_finish(const FinishParams p) {
 
   // 3. collapse, kept in registers as BF16 for the normalisation
   const float p0 = pre_s[0], p1 = pre_s[1], p2 = pre_s[2], p3 = pre_s[3];
-  uint4 cfr[MAXF];
+  uint4 cfr[NF];
   float ssq = 0.f;
 #pragma unroll
-  for (int i = 0; i < MAXF; ++i) {
-    const int fr = tid + i * NT;
-    cfr[i] = make_uint4(0u, 0u, 0u, 0u);
-    if (fr < nfrag) {
-      float n0[8], n1[8], n2[8], n3[8], c[8];
-      const uint16_t *s = p.streams + (size_t)t * HC * H + (size_t)fr * VEC;
-      unpack8(ld_vec(s), n0);
-      unpack8(ld_vec(s + H), n1);
-      unpack8(ld_vec(s + 2 * (size_t)H), n2);
-      unpack8(ld_vec(s + 3 * (size_t)H), n3);
+  for (int i = 0; i < NF; ++i) {
+    float n0[8], n1[8], n2[8], n3[8], c[8];
+    unpack8(sv[i][0], n0);
+    unpack8(sv[i][1], n1);
+    unpack8(sv[i][2], n2);
+    unpack8(sv[i][3], n3);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], p0), __fmul_rn(n1[e], p1)),
-                         __fadd_rn(__fmul_rn(n2[e], p2), __fmul_rn(n3[e], p3)));
-      cfr[i] = round8(c);
+    for (int e = 0; e < 8; ++e)
+      c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], p0), __fmul_rn(n1[e], p1)),
+                       __fadd_rn(__fmul_rn(n2[e], p2), __fmul_rn(n3[e], p3)));
+    cfr[i] = round8(c);   // fragments past H hold zeros and add nothing
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
-    }
+    for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
   }
   ssq = warp_sum(ssq);
   if (lane == 0) red_s[warp] = ssq;
@@ -135,9 +150,8 @@ __global__ void __launch_bounds__(NT) k_finish(const FinishParams p) {
   // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
   const int cols = H / 32;
 #pragma unroll
-  for (int i = 0; i < MAXF; ++i) {
+  for (int i = 0; i < NF; ++i) {
     const int fr = tid + i * NT;
-    if (i * NT >= nfrag) break;          // uniform over the CTA
     const bool live = fr < nfrag;
     float o[8];
     uint4 ob = make_uint4(0u, 0u, 0u, 0u);
@@ -183,17 +197,24 @@ __global__ void __launch_bounds__(NT) k_finish(const FinishParams p) {
 }  // namespace
 
 cudaError_t launch_finish(const FinishParams &p, cudaStream_t stream, bool pdl) {
+  using Kernel = void (*)(FinishParams);
+  static const Kernel kernels[MAXF] = {k_finish<1>, k_finish<2>, k_finish<3>, k_finish<4>,
+                                       k_finish<5>, k_finish<6>, k_finish<7>, k_finish<8>};
+  const int nf = (p.hidden / VEC + NT - 1) / NT;
+  if (nf < 1 || nf > MAXF) return cudaErrorInvalidValue;
+  const size_t smem = size_t(p.slices) * VALUES * sizeof(float);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.m);
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_finish, p);
+  return cudaLaunchKernelEx(&cfg, kernels[nf - 1], p);
 }
 
 }  // namespace mhc

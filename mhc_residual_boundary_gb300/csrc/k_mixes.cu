@@ -1,6 +1,6 @@
 // k_mixes.cu -- side-stream kernel: the next boundary's post-mix and Sinkhorn
-// residual mix from this boundary's raw mixes, one thread per token, one warp
-// per CTA ([GLM] _MixesDeviceKernel.kernel and _MixesDeviceKernel._sinkhorn).
+// residual mix from this boundary's raw mixes ([GLM] _MixesDeviceKernel.kernel
+// and _MixesDeviceKernel._sinkhorn).
 //
 //   post_j = sigmoid(mixes_{4+j} * scale[1] + base[4+j]) * post_mult
 //   logits c[r][k] = mixes_{8+4r+k} * scale[2] + base[8+4r+k]
@@ -8,7 +8,14 @@
 //   `repeat` rounds: (from the second round) rows c /= (row sum + eps);
 //                    columns c /= (column sum + eps)
 // with the four-term sums paired ((a + b) + (c + d)) and 1/x reciprocals, as
-// on the page.  The matrix lives in 16 registers.
+// on the page.
+//
+// The rounds are a chain of dependent steps per token, so the kernel spreads
+// a token over 16 lanes, one matrix element each (lane 4r + k of the token's
+// half-warp): a row sum is two butterfly shuffles over lanes 4r .. 4r+3
+// (xor 1 then xor 2 gives (c0 + c1) + (c2 + c3) on every lane of the row), a
+// column sum two over lanes k, k+4, k+8, k+12 (xor 4 then xor 8).  Lanes 0-3
+// of the token also compute post.  Two tokens per warp, eight per CTA.
 //
 // Page: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc.
 #include "device_common.cuh"
@@ -17,59 +24,48 @@
 namespace mhc {
 namespace {
 
+constexpr int NT = 128;
+constexpr int LANES = HC * HC;             // lanes per token
+constexpr int TOKENS = NT / LANES;         // tokens per CTA
+
 __device__ __forceinline__ float sigmoid(float z) {
   return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
 }
 
-__global__ void __launch_bounds__(32) k_mixes(const MixesParams p) {
-  const int t = blockIdx.x * 32 + threadIdx.x;
-  if (t >= p.m) return;
-  const float *row = p.mixes + (size_t)t * MIX;
-  const float s1 = p.scale[1], s2 = p.scale[2], eps = p.eps;
-#pragma unroll
-  for (int j = 0; j < HC; ++j) {
-    const float z = __fadd_rn(__fmul_rn(row[HC + j], s1), p.base[HC + j]);
-    p.post_out[(size_t)t * HC + j] = __fmul_rn(sigmoid(z), p.post_mult);
+// Paired four-term sum over the lanes that differ in bits a and 2a.
+__device__ __forceinline__ float sum4(float x, int a) {
+  const float s = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, a));
+  return __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2 * a));
+}
+
+__global__ void __launch_bounds__(NT) k_mixes(const MixesParams p) {
+  const int e = threadIdx.x & (LANES - 1);        // element 4r + k
+  const int t = blockIdx.x * TOKENS + threadIdx.x / LANES;
+  // the whole warp runs the shuffles; lanes of a token past m compute on zeros
+  const bool live = t < p.m;
+  const float *row = p.mixes + (size_t)(live ? t : 0) * MIX;
+  if (live && e < HC) {
+    const float z = __fadd_rn(__fmul_rn(row[HC + e], p.scale[1]), p.base[HC + e]);
+    p.post_out[(size_t)t * HC + e] = __fmul_rn(sigmoid(z), p.post_mult);
   }
-  float c[HC * HC];
-#pragma unroll
-  for (int i = 0; i < HC * HC; ++i) c[i] = __fadd_rn(__fmul_rn(row[2 * HC + i], s2), p.base[2 * HC + i]);
-#pragma unroll
-  for (int r = 0; r < HC; ++r) {
-    float *x = c + r * HC;
-    const float peak = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-    for (int k = 0; k < HC; ++k) x[k] = expf(__fsub_rn(x[k], peak));
-    const float inv = __frcp_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])));
-#pragma unroll
-    for (int k = 0; k < HC; ++k) x[k] = __fadd_rn(__fmul_rn(x[k], inv), eps);
-  }
+  const float eps = p.eps;
+  float x = live ? __fadd_rn(__fmul_rn(row[2 * HC + e], p.scale[2]), p.base[2 * HC + e]) : 0.f;
+  // row softmax
+  float peak = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  peak = fmaxf(peak, __shfl_xor_sync(0xffffffffu, peak, 2));
+  x = expf(__fsub_rn(x, peak));
+  x = __fadd_rn(__fmul_rn(x, __frcp_rn(sum4(x, 1))), eps);
   for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) {
-#pragma unroll
-      for (int r = 0; r < HC; ++r) {
-        float *x = c + r * HC;
-        const float inv = __frcp_rn(__fadd_rn(__fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3])), eps));
-#pragma unroll
-        for (int k = 0; k < HC; ++k) x[k] = __fmul_rn(x[k], inv);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < HC; ++k) {
-      const float inv = __frcp_rn(__fadd_rn(
-          __fadd_rn(__fadd_rn(c[k], c[HC + k]), __fadd_rn(c[2 * HC + k], c[3 * HC + k])), eps));
-#pragma unroll
-      for (int r = 0; r < HC; ++r) c[r * HC + k] = __fmul_rn(c[r * HC + k], inv);
-    }
+    if (it > 0) x = __fmul_rn(x, __frcp_rn(__fadd_rn(sum4(x, 1), eps)));
+    x = __fmul_rn(x, __frcp_rn(__fadd_rn(sum4(x, HC), eps)));
   }
-#pragma unroll
-  for (int i = 0; i < HC * HC; ++i) p.comb_out[(size_t)t * HC * HC + i] = c[i];
+  if (live) p.comb_out[(size_t)t * LANES + e] = x;
 }
 
 }  // namespace
 
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream) {
-  k_mixes<<<(p.m + 31) / 32, 32, 0, stream>>>(p);
+  k_mixes<<<(p.m + TOKENS - 1) / TOKENS, NT, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

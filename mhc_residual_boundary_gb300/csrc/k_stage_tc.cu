@@ -167,8 +167,8 @@ __device__ __forceinline__ void load_item(int tp, const unsigned char *st, int t
 
 // Stage 1 and post-mix of two items in one instruction stream; returns the
 // stage-1 sums and the new streams as BF16 fragments and each item's sum of
-// squares.  The FP32 arithmetic runs on element pairs (packed add / mul /
-// fma, each lane rounded to nearest as the scalar operation would be).
+// squares.  The post-mix runs on FP32 element pairs (packed mul / fma, each
+// lane rounded to nearest as the scalar operation would be).
 __device__ __forceinline__ void mix_pair(int tp, const Item (&it)[2], uint4 (&yb)[2], uint4 (&nv)[2][HC],
                                          float (&ss)[2]) {
   float2 y[2][4];
@@ -181,10 +181,13 @@ __device__ __forceinline__ void mix_pair(int tp, const Item (&it)[2], uint4 (&yb
     if (q < tp) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        float2 x[4];
-        unpack4x2(it[k].part[q], x);
+        // FP32 += BF16 with the widening folded into the add (exact, so
+        // each lane rounds once, as the FP32 add of the widened value would)
+        const uint32_t ww[4] = {it[k].part[q].x, it[k].part[q].y, it[k].part[q].z, it[k].part[q].w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[k][e] = __fadd2_rn(y[k][e], x[e]);
+        for (int e = 0; e < 4; ++e)
+          asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;}"
+              : "+f"(y[k][e].x), "+f"(y[k][e].y) : "r"(ww[e]));
       }
     }
   }
