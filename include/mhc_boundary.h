@@ -220,7 +220,7 @@ size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden);
  * so post_out / comb_out need no join.
  * Scratch: an 8 MiB array of this library's device memory, which every GPU
  * that loads the library holds until the process exits; a call needs
- * m * (25 * ceil(H / 64) + 24) * 4 + 256 bytes of it (H = 6144: up to 865 tokens),
+ * m * (4 * ceil(25 * ceil(H / 64) / 4) + 24) * 4 + 256 bytes of it (H = 6144: up to 865 tokens),
  * and a larger m returns MHC_ERR_CAPACITY with nothing launched.  Every call
  * on a device shares that array and it keeps the last call's contents
  * (nothing needs clearing: each call writes every word it reads before

@@ -33,7 +33,7 @@ struct mhc_boundary {
   cudaEvent_t side_done = nullptr;
   bool side_pending = false;
   float *mixes = nullptr;        // [cap][24] raw mixes read by the side kernel
-  float *part = nullptr;         // [cap][slices][25] stage-kernel partial sums
+  float *part = nullptr;         // [cap][part_row_floats(slices)] stage-kernel partial sums
   unsigned int *err = nullptr;   // device-detected argument errors
   unsigned char *staging = nullptr;
   size_t staging_bytes = 0;
@@ -164,6 +164,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = b->part;
+  sp.part_stride = part_row_floats(sp.slices);
   sp.err = b->err;
   e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, moe != nullptr, stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
@@ -177,6 +178,8 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   fp.hidden = c.hidden;
   fp.slices = sp.slices;
   fp.part = b->part;
+  fp.part_stride = sp.part_stride;
+  fp.err = b->err;
   fp.scale = a->scale;
   fp.base = a->base;
   fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
@@ -190,7 +193,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   fp.layer_input = static_cast<uint16_t *>(a->layer_input);
   fp.mx_values = a->mxfp8_values;
   fp.mx_scales = a->mxfp8_scales;
-  e = launch_finish(fp, stream, ev == nullptr);
+  e = launch_finish(fp, b->sm_count, stream, ev == nullptr);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
   if (ev) cudaEventRecord(ev[3], stream);
 
@@ -316,6 +319,7 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   const size_t cap = size_t(c.max_num_tokens);
   cudaError_t e = stage_set_attributes();
   if (e == cudaSuccess) e = stage_tc_set_attributes();
+  if (e == cudaSuccess) e = finish_set_attributes();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b->sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->main_ready, cudaEventDisableTiming);
@@ -326,7 +330,7 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
     return fail(g_create_error, MHC_ERR_CUDA, "create: %s", cudaGetErrorString(e));
   }
   e = cudaMalloc(&b->mixes, cap * MIX * sizeof(float));
-  if (e == cudaSuccess) e = cudaMalloc(&b->part, cap * b->slices * VALUES * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&b->part, cap * part_row_floats(b->slices) * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&b->err, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(b->err, 0, sizeof(unsigned int));
   if (e == cudaSuccess && (c.flags & MHC_FLAG_HOST_STAGING)) {

@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
     } else {
       s = ss_s[tl2];
     }
-    p.part[((size_t)tok * p.slices + slice) * VALUES + v] = s;
+    p.part[(size_t)tok * p.part_stride + slice * VALUES + v] = s;
   }
 }
 

@@ -36,8 +36,8 @@
 //     token; warp q reads outputs 0-11 and warp q + 4 outputs 12-23 of all
 //     four blocks, the four streams of a token are added in the order
 //     ((j0 + j1) + (j2 + j3)) with warp shuffles, and the sums go to the
-//     scratch [m][groups][25] (24 sums + the sum of squares) that the finish
-//     kernel reduces.
+//     scratch rows [m][groups][25] (24 sums + the sum of squares; rows padded
+//     to 16 bytes) that the finish kernel reduces.
 // Every wait is bounded; a wait that gives up sets bit 1 of the error word.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
@@ -258,7 +258,7 @@ __device__ __forceinline__ void epilogue(const StageParams &p, uint32_t tmem, ui
   }
   const int t = tile * UT + q * QT + (lane >> 2);
   if (ok && t < p.m) {
-    float *dst = p.part + ((size_t)t * p.slices + grpc) * VALUES + OUT_HALF * half + 3 * j;
+    float *dst = p.part + (size_t)t * p.part_stride + grpc * VALUES + OUT_HALF * half + 3 * j;
     dst[0] = out[0];
     dst[1] = out[1];
     dst[2] = out[2];
@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(NT, 1)
       load_item(p.tp, stage, tl[0], f, it[0]);
       load_item(p.tp, stage, tl[1], f, it[1]);
     }
+    // The slot's next fill is an async-proxy write: the generic-proxy reads
+    // above are ordered before it by a proxy fence ahead of the release.
+    tc::fence_proxy_async_smem();
     tc::mbar_arrive(&empty[q]);
     // once both warps of the slot hold unit i's stage, the slot takes unit i + 1's
     if (filler && ok && i + 1 < n_units) {
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(NT, 1)
       s += __shfl_xor_sync(0xffffffffu, s, 4);
       s += __shfl_xor_sync(0xffffffffu, s, 8);
       const int t = tile * UT + q * QT + tl[k];
-      if (f == 0 && ok && t < p.m) p.part[((size_t)t * G + gc) * VALUES + MIX] = s;
+      if (f == 0 && ok && t < p.m) p.part[(size_t)t * p.part_stride + gc * VALUES + MIX] = s;
     }
     pending = -1;
     // hand the A buffer to the tensor core

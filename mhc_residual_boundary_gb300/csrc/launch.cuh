@@ -19,6 +19,9 @@ constexpr int TC_GROUP_COLS = 128;
 // Ranks one TMA box of the tensor-core stage kernel covers; calls with more
 // partials run the CUDA-core stage kernel.
 constexpr int TP_TMA_MAX = 8;
+// Floats per token row of the partial-sum scratch: slices x 25, padded to a
+// multiple of 4 so that every row starts on a 16-byte boundary.
+constexpr int part_row_floats(int slices) { return (slices * VALUES + 3) / 4 * 4; }
 // Dynamic shared memory the stage kernel may use (of 227 KB per CTA).
 constexpr size_t STAGE_SMEM_LIMIT = 200 * 1024;
 // Largest hidden size the finish kernel's register tiling covers.
@@ -40,7 +43,8 @@ struct StageParams {
   const float *hc_fn;         // [4H][24]
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
-  float *part;                // [m][slices][25] partial GEMV outputs + sum of squares
+  float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares
+  int part_stride;            // floats per token row of part (part_row_floats(slices))
   unsigned int *err;          // device error word (bit 0: bad route index,
                               // bit 1: a tensor-core completion wait gave up)
 };
@@ -48,7 +52,7 @@ struct StageParams {
 // Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm
 // and the optional MXFP8 copy.
 struct FinishParams {
-  int m, hidden, slices;
+  int m, hidden, slices, part_stride;
   const float *part;
   const float *scale;
   const float *base;
@@ -61,6 +65,7 @@ struct FinishParams {
   uint16_t *layer_input;      // [m][H]
   uint8_t *mx_values;         // [m][H] or null
   uint8_t *mx_scales;         // mxfp8_scale_bytes(m, H) or null
+  unsigned int *err;          // device error word (bit 1: a wait gave up) or null
 };
 
 // Side kernel: post-mix and Sinkhorn residual mix of the next boundary.
@@ -84,7 +89,10 @@ cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream);
 size_t stage_tc_smem_bytes();
 cudaError_t stage_tc_set_attributes();
 cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream);
-cudaError_t launch_finish(const FinishParams &p, cudaStream_t stream, bool pdl);
+// Finish kernel: persistent CTAs (at most `ctas`), programmatic dependent
+// launch after the stage kernel when `pdl`.
+cudaError_t finish_set_attributes();
+cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
 
 }  // namespace mhc

@@ -30,7 +30,8 @@ using namespace mhc;
 
 namespace {
 
-// Scratch of every call: [m][slices][25] partial sums, then [m][24] mixes.
+// Scratch of every call: [m] rows of partial sums ([slices][25] padded to a
+// multiple of 4 floats), then [m][24] mixes.
 constexpr size_t STATIC_SCRATCH_BYTES = size_t(8) << 20;   // 8 MiB per device
 __device__ __align__(256) float g_scratch[STATIC_SCRATCH_BYTES / sizeof(float)];
 
@@ -67,6 +68,7 @@ mhc_status_t scratch_on_device(int device, float **out, char *error, size_t erro
       cudaError_t e = cudaGetSymbolAddress(&addr, g_scratch);
       if (e == cudaSuccess) e = stage_set_attributes();
       if (e == cudaSuccess) e = stage_tc_set_attributes();
+      if (e == cudaSuccess) e = finish_set_attributes();
       if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sm_count[device], cudaDevAttrMultiProcessorCount, device);
       if (e != cudaSuccess)
         return report(error, error_len, MHC_ERR_CUDA, "set-up on device %d: %s", device, cudaGetErrorString(e));
@@ -98,7 +100,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
     return report(error, error_len, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
 
   const int slices = (c.hidden + SLICE - 1) / SLICE;
-  const size_t per_token = size_t(slices) * VALUES + MIX;    // floats
+  const size_t per_token = size_t(part_row_floats(slices)) + MIX;    // floats
   // the mixes start at a 64-float boundary after the partial sums
   const size_t max_m = (STATIC_SCRATCH_BYTES / sizeof(float) - 64) / per_token;
   if (a->m < 1 || size_t(a->m) > max_m)
@@ -140,7 +142,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   // the CUDA-core one per 64; the capacity rule above counts the latter
   const bool tc_path = c.tp <= TP_TMA_MAX;
   const int groups = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : slices;
-  float *mixes = scratch + (size_t(a->m) * groups * VALUES + 63) / 64 * 64;
+  float *mixes = scratch + (size_t(a->m) * part_row_floats(groups) + 63) / 64 * 64;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
   StageParams sp = {};
@@ -156,6 +158,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;
+  sp.part_stride = part_row_floats(groups);
   sp.err = nullptr;   // read only by the MoE variant, which this entry point does not run
   e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream) : launch_stage(sp, false, stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
@@ -165,6 +168,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   fp.hidden = c.hidden;
   fp.slices = groups;
   fp.part = part;
+  fp.part_stride = sp.part_stride;
   fp.scale = a->scale;
   fp.base = a->base;
   fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
@@ -178,7 +182,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   fp.layer_input = static_cast<uint16_t *>(a->layer_input);
   fp.mx_values = a->mxfp8_values;
   fp.mx_scales = a->mxfp8_scales;
-  e = launch_finish(fp, stream, true);
+  e = launch_finish(fp, g_sm_count[device], stream, true);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
 
   MixesParams mp = {};

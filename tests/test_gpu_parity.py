@@ -66,7 +66,11 @@ def test_large_mxfp8(Boundary):
 
 
 @pytest.mark.parametrize("hidden,tp,m", [(8, 1, 1), (8, 3, 9), (72, 2, 17), (520, 5, 33),
-                                         (1000, 8, 300), (128, 1, 129)])
+                                         (1000, 8, 300), (128, 1, 129),
+                                         # more partials than one tensor-map box: CUDA-core stage kernel
+                                         (1024, 12, 50),
+                                         # the largest hidden size: one finish ring slot per CTA
+                                         (16384, 8, 40)])
 def test_ragged_shapes(Boundary, hidden, tp, m):
     check(Boundary, hidden, tp, m, seed=hidden + m)
 
