@@ -173,7 +173,13 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
  * first makes `stream` wait for the previous call's side-stream kernel (the
  * automatic join), then launches the main kernels on `stream` and the
  * post / Sinkhorn kernel on the side stream.  post_out and comb_out are valid
- * for `stream` only after mhc_boundary_join (or the next call). */
+ * for `stream` only after mhc_boundary_join (or the next call).
+ * Stream capture: calls may be recorded into a CUDA graph.  Inside a capture
+ * the automatic join covers only side kernels of the same capture, so join
+ * and finish eager calls before the capture begins, and call
+ * mhc_boundary_join on the capturing stream before ending the capture (the
+ * side stream's branch must rejoin it).  Profiling events are not recorded
+ * inside a capture. */
 mhc_status_t mhc_boundary_run(mhc_boundary_t *b, const mhc_run_args_t *args,
                               mhc_stream_t stream);
 
@@ -182,20 +188,23 @@ mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *
                                        mhc_stream_t stream);
 
 /* Makes `stream` wait for the last side-stream kernel ([GLM]
- * AllReduceMhcBoundary.join).  Cheap; may be called any number of times. */
+ * AllReduceMhcBoundary.join).  Cheap; may be called any number of times.
+ * On a capturing stream it joins a side kernel of the same capture; a side
+ * kernel that ran in a captured graph is ordered by the graph itself. */
 mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream);
 
 /* mhc_boundary_run with HOST pointers in `args` (every tensor in host
  * memory; pinned memory makes the copies asynchronous).  Needs
  * MHC_FLAG_HOST_STAGING.  Copies the inputs to library staging buffers on
  * `stream`, runs, joins, copies the outputs back and synchronises `stream`
- * before returning. */
+ * before returning (so it cannot be captured). */
 mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *args,
                                    mhc_stream_t stream);
 
 /* Synchronises the handle's streams and reports device-detected errors of
- * earlier calls: MHC_ERR_TIMEOUT if a stage kernel gave up its bounded wait
- * for tensor-core work (its outputs are then invalid), MHC_ERR_INVALID_ARG
+ * earlier calls: MHC_ERR_TIMEOUT if a kernel gave up one of its bounded
+ * waits (for copies or tensor-core work; its outputs are then invalid),
+ * MHC_ERR_INVALID_ARG
  * for an out-of-range MoE route index, else MHC_OK (the flags are cleared). */
 mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b);
 

@@ -32,6 +32,9 @@ struct mhc_boundary {
   cudaEvent_t main_ready = nullptr;
   cudaEvent_t side_done = nullptr;
   bool side_pending = false;
+  // capture id of the stream capture side_done was last recorded in (0: none);
+  // a call inside a capture waits only for side kernels of the same capture
+  unsigned long long side_capture = 0;
   float *mixes = nullptr;        // [cap][24] raw mixes read by the side kernel
   float *part = nullptr;         // [cap][part_row_floats(slices)] stage-kernel partial sums
   unsigned int *err = nullptr;   // device-detected argument errors
@@ -129,14 +132,34 @@ mhc_status_t validate_moe(const mhc_boundary *b, const mhc_moe_args_t *a, std::s
   return MHC_OK;
 }
 
+// The id of the capture `stream` is recording into, 0 when it is not capturing.
+cudaError_t capture_id(cudaStream_t stream, unsigned long long *id) {
+  cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
+  *id = 0;
+  const cudaError_t e = cudaStreamGetCaptureInfo(stream, &status, id);
+  if (status != cudaStreamCaptureStatusActive) *id = 0;
+  return e;
+}
+
+// Whether work on a stream in capture `capture` (0: none) must wait for the
+// last side kernel: always outside a capture, unless that kernel was itself
+// captured (a graph orders its own side branch); inside a capture only when
+// it was recorded in the same capture (an earlier eager call must have been
+// joined before the capture began).
+bool side_join_needed(const mhc_boundary *b, unsigned long long capture) {
+  if (!b->side_pending) return false;
+  return capture == 0 ? b->side_capture == 0 : b->side_capture == capture;
+}
+
 mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe_args_t *moe,
                          cudaStream_t stream) {
   const mhc_boundary_config_t &c = b->cfg;
-  cudaError_t e = cudaSuccess;
-  if (b->side_pending) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+  unsigned long long capture = 0;
+  cudaError_t e = capture_id(stream, &capture);
+  if (e == cudaSuccess && side_join_needed(b, capture)) e = cudaStreamWaitEvent(stream, b->side_done, 0);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "join: %s", cudaGetErrorString(e));
-  cudaEvent_t *ev = nullptr;   // 6 events of this call when profiling
-  if (b->prof_calls < b->prof_capacity) ev = &b->prof_events[size_t(b->prof_calls) * 6];
+  cudaEvent_t *ev = nullptr;   // 6 events of this call when profiling (never inside a capture)
+  if (capture == 0 && b->prof_calls < b->prof_capacity) ev = &b->prof_events[size_t(b->prof_calls) * 6];
   const bool sync_mixes = (c.flags & MHC_FLAG_SYNC_MIXES) != 0;
   if (ev) cudaEventRecord(ev[0], stream);
 
@@ -219,6 +242,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
   if (ev) ++b->prof_calls;
   b->side_pending = true;
+  b->side_capture = capture;
   b->last_error.clear();
   return MHC_OK;
 }
@@ -377,7 +401,10 @@ mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream) {
   if (!b) return MHC_ERR_INVALID_ARG;
   if (!b->side_pending) return MHC_OK;
   DeviceGuard guard(b->device);
-  const cudaError_t e = cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), b->side_done, 0);
+  unsigned long long capture = 0;
+  cudaError_t e = capture_id(reinterpret_cast<cudaStream_t>(stream), &capture);
+  if (e == cudaSuccess && side_join_needed(b, capture))
+    e = cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), b->side_done, 0);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "join: %s", cudaGetErrorString(e));
   return MHC_OK;
 }
@@ -464,7 +491,7 @@ mhc_status_t mhc_boundary_check_errors(mhc_boundary_t *b) {
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "check_errors: %s", cudaGetErrorString(e));
   if (flag & 2u)
     return fail(b->last_error, MHC_ERR_TIMEOUT,
-                "a stage kernel gave up waiting for its tensor-core work; its outputs are not valid");
+                "a kernel gave up one of its bounded waits (copies or tensor-core work); its outputs are not valid");
   if (flag & 1u)
     return fail(b->last_error, MHC_ERR_INVALID_ARG,
                 "a MoE route index was outside [-1, rows_per_rank); the route was skipped");

@@ -104,16 +104,28 @@ __device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 0;" ::: "mem
 
 // The group's hc_fn as three BF16 B operands (hi, mid, lo), K-major core
 // matrices [term][core column][8-column block][8 columns][8 inputs];
-// column n = stream * 24 + output, input k = column in the group.
-__device__ void build_b(const StageParams &p, int h0, unsigned char *b_s) {
-  for (int e = threadIdx.x; e < (UK / 2) * UN; e += NT) {
+// column n = stream * 24 + output, input k = column in the group.  Every
+// thread issues all its loads before the first split, so the build costs
+// one memory latency rather than one per element pair.
+constexpr int B_PAIRS = (UK / 2) * UN / NT;   // element pairs per thread
+static_assert((UK / 2) * UN % NT == 0, "B build split");
+__device__ __noinline__ void build_b(const StageParams &p, int h0, unsigned char *b_s) {
+  float x0[B_PAIRS], x1[B_PAIRS];
+#pragma unroll
+  for (int it = 0; it < B_PAIRS; ++it) {
+    const int e = threadIdx.x + it * NT;
     const int kp = e / UN, n = e % UN, j = n / MIX, i = n % MIX;
-    const int k = 2 * kp, h = h0 + k;
+    const int h = h0 + 2 * kp;
     const float *src = p.hc_fn + ((size_t)j * p.hidden + h) * MIX + i;
-    const float x0 = h < p.hidden ? __ldg(src) : 0.f;
-    const float x1 = h + 1 < p.hidden ? __ldg(src + MIX) : 0.f;
-    const uint32_t hi = pack_bf16x2(x0, x1);
-    const float r0 = __fsub_rn(x0, bf16_lo(hi)), r1 = __fsub_rn(x1, bf16_hi(hi));
+    x0[it] = h < p.hidden ? __ldg(src) : 0.f;
+    x1[it] = h + 1 < p.hidden ? __ldg(src + MIX) : 0.f;
+  }
+#pragma unroll
+  for (int it = 0; it < B_PAIRS; ++it) {
+    const int e = threadIdx.x + it * NT;
+    const int kp = e / UN, n = e % UN, k = 2 * kp;
+    const uint32_t hi = pack_bf16x2(x0[it], x1[it]);
+    const float r0 = __fsub_rn(x0[it], bf16_lo(hi)), r1 = __fsub_rn(x1[it], bf16_hi(hi));
     const uint32_t mid = pack_bf16x2(r0, r1);
     const uint32_t lo = pack_bf16x2(__fsub_rn(r0, bf16_lo(mid)), __fsub_rn(r1, bf16_hi(mid)));
     const size_t inner = size_t(n / 8) * 128 + (n % 8) * 16 + (k % 8) * 2;
