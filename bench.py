@@ -363,7 +363,7 @@ def run_ours(args, w):
                "cores": threads, "kind": "oracle",
                "sample": f"all {sample} tokens of the workload once, token ranges over {threads} threads"}
 
-    launches = b.launches_per_call()
+    launches = b.launches_per_call() + (1 if w.moe else 0)
     b.close()
     if rank == 0:
         print(json.dumps({
@@ -430,7 +430,7 @@ def run_sweep(args):
             # the same calls replayed from a CUDA graph: device time without
             # the Python binding's per-call host cost
             graph_us = None
-            if nsets <= 64:
+            if nsets <= 512:
                 cap = torch.cuda.Stream()
                 cap.wait_stream(stream)
                 g = torch.cuda.CUDAGraph()

@@ -70,13 +70,20 @@ enum {
   /* Accept mxfp8_values / mxfp8_scales (needs hidden % 128 == 0);
    * [DSV] AllReduceMHC(quantize_layer_input=True). */
   MHC_FLAG_MXFP8 = 1u << 0,
-  /* Run the post / Sinkhorn kernel on the caller's stream instead of the
-   * library side stream: post_out / comb_out are then ordered like every
-   * other output and join() is a no-op. */
+  /* Compute post / Sinkhorn in a separate one-warp-per-32-tokens kernel on
+   * the caller's stream (takes precedence over MHC_FLAG_SIDE_MIXES).  Without
+   * either flag the finish kernel computes them itself, on the caller's
+   * stream, beside the collapse of the same token.  All three forms give the
+   * same bits; with no side stream, join() is a no-op. */
   MHC_FLAG_SYNC_MIXES = 1u << 1,
   /* Allocate device staging buffers in create so that mhc_boundary_run_host
    * can take host pointers. */
-  MHC_FLAG_HOST_STAGING = 1u << 2
+  MHC_FLAG_HOST_STAGING = 1u << 2,
+  /* [GLM] AllReduceMhcBoundary's layout: post / Sinkhorn in a separate kernel
+   * on the library side stream, so that they overlap whatever the caller
+   * enqueues next; post_out / comb_out are then valid only after
+   * mhc_boundary_join (or the next call, which joins automatically). */
+  MHC_FLAG_SIDE_MIXES = 1u << 3
 };
 
 /* Construction arguments ([GLM] AllReduceMhcBoundary.__init__, [DSV]
@@ -169,11 +176,13 @@ typedef struct {
 mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device,
                                  mhc_boundary_t **out);
 
-/* One boundary call on `stream` ([GLM] AllReduceMhcBoundary.__call__).  It
+/* One boundary call on `stream` ([GLM] AllReduceMhcBoundary.__call__): the
+ * stage and finish kernels on `stream`; post / Sinkhorn inside the finish
+ * kernel, or (flags) in a separate kernel.  With MHC_FLAG_SIDE_MIXES the call
  * first makes `stream` wait for the previous call's side-stream kernel (the
- * automatic join), then launches the main kernels on `stream` and the
- * post / Sinkhorn kernel on the side stream.  post_out and comb_out are valid
- * for `stream` only after mhc_boundary_join (or the next call).
+ * automatic join) and post_out / comb_out are valid for `stream` only after
+ * mhc_boundary_join (or the next call); otherwise they are ordered like every
+ * other output.
  * Stream capture: calls may be recorded into a CUDA graph.  Inside a capture
  * the automatic join covers only side kernels of the same capture, so join
  * and finish eager calls before the capture begins, and call
@@ -183,7 +192,10 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
 mhc_status_t mhc_boundary_run(mhc_boundary_t *b, const mhc_run_args_t *args,
                               mhc_stream_t stream);
 
-/* mhc_boundary_run with the MoE fold as stage 1 (needs top_k > 0). */
+/* mhc_boundary_run with the MoE fold as stage 1 (needs top_k > 0): a fold
+ * kernel writes the stage-1 sum to library scratch ([cap][H] bf16, allocated
+ * in create when top_k > 0), which the stage kernel reads as its only
+ * partial. */
 mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *args,
                                        mhc_stream_t stream);
 
@@ -259,7 +271,9 @@ mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls);
  * recording (the events are destroyed). */
 mhc_status_t mhc_boundary_profile_end(mhc_boundary_t *b, mhc_profile_t *out);
 
-/* Kernels one run / finalize_moe call launches (main stream + side stream). */
+/* Kernels one mhc_boundary_run call launches: stage + finish, plus the
+ * post / Sinkhorn kernel with MHC_FLAG_SIDE_MIXES or MHC_FLAG_SYNC_MIXES.
+ * mhc_boundary_finalize_moe launches one more (the MoE fold). */
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b);
 
 const char *mhc_status_string(mhc_status_t status);

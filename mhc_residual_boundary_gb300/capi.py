@@ -20,6 +20,7 @@ STATUS = {0: "MHC_OK", 1: "MHC_ERR_INVALID_ARG", 2: "MHC_ERR_UNSUPPORTED", 3: "M
 MHC_FLAG_MXFP8 = 1 << 0
 MHC_FLAG_SYNC_MIXES = 1 << 1
 MHC_FLAG_HOST_STAGING = 1 << 2
+MHC_FLAG_SIDE_MIXES = 1 << 3
 
 
 class MhcError(RuntimeError):

@@ -37,6 +37,7 @@ struct mhc_boundary {
   unsigned long long side_capture = 0;
   float *mixes = nullptr;        // [cap][24] raw mixes read by the side kernel
   float *part = nullptr;         // [cap][part_row_floats(slices)] stage-kernel partial sums
+  uint16_t *fold = nullptr;      // [cap][H] bf16 stage-1 sum of MoE calls (top_k > 0)
   unsigned int *err = nullptr;   // device-detected argument errors
   unsigned char *staging = nullptr;
   size_t staging_bytes = 0;
@@ -167,19 +168,31 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.m = a->m;
   sp.hidden = c.hidden;
   sp.tp = c.tp;
-  // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
-  // groups (tensor-core kernel); the scratch holds the larger count
-  const bool tc_path = moe == nullptr && c.tp <= TP_TMA_MAX;
-  sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
   sp.partials = static_cast<const uint16_t *>(a->partials);
   if (moe) {
-    sp.routed = static_cast<const uint16_t *>(moe->routed);
-    sp.idx = moe->idx;
-    sp.weights = moe->weights;
-    sp.shared = static_cast<const uint16_t *>(moe->shared);
-    sp.top_k = c.top_k;
-    sp.rows_per_rank = moe->rows_per_rank;
+    // stage 1 of a MoE call: the fold kernel writes y, which the
+    // tensor-core stage kernel then takes as its single partial
+    FoldParams fo = {};
+    fo.m = a->m;
+    fo.hidden = c.hidden;
+    fo.tp = c.tp;
+    fo.top_k = c.top_k;
+    fo.rows_per_rank = moe->rows_per_rank;
+    fo.routed = static_cast<const uint16_t *>(moe->routed);
+    fo.idx = moe->idx;
+    fo.weights = moe->weights;
+    fo.shared = static_cast<const uint16_t *>(moe->shared);
+    fo.y = b->fold;
+    fo.err = b->err;
+    e = launch_moe_fold(fo, b->sm_count * 16, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
+    sp.tp = 1;
+    sp.partials = b->fold;
   }
+  // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
+  // groups (tensor-core kernel); the scratch holds the larger count
+  const bool tc_path = sp.tp <= TP_TMA_MAX;
+  sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
   sp.residual = static_cast<const uint16_t *>(a->residual);
   sp.post = a->post;
   sp.comb = a->comb;
@@ -189,7 +202,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.part = b->part;
   sp.part_stride = part_row_floats(sp.slices);
   sp.err = b->err;
-  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, moe != nullptr, stream);
+  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, false, stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
   if (ev) {
     cudaEventRecord(ev[1], stream);
@@ -210,9 +223,17 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   fp.rms_eps = c.rms_eps;
   fp.hc_eps = c.hc_eps;
   fp.norm_eps = c.norm_eps;
-  fp.mixes = b->mixes;
+  // post / Sinkhorn: in the finish kernel (default), or a separate kernel on
+  // the side stream ([GLM] design) or on the caller's stream
+  const bool separate = (c.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) != 0;
+  const bool on_side = separate && !sync_mixes;
+  fp.mixes = separate ? b->mixes : nullptr;
   fp.mixes_out = a->mixes_out;
   fp.pre_out = a->pre_out;
+  fp.post_out = separate ? nullptr : a->post_out;
+  fp.comb_out = separate ? nullptr : a->comb_out;
+  fp.post_mult = c.post_mult;
+  fp.repeat = c.sinkhorn_repeat;
   fp.layer_input = static_cast<uint16_t *>(a->layer_input);
   fp.mx_values = a->mxfp8_values;
   fp.mx_scales = a->mxfp8_scales;
@@ -220,29 +241,37 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
   if (ev) cudaEventRecord(ev[3], stream);
 
-  MixesParams mp = {};
-  mp.m = a->m;
-  mp.repeat = c.sinkhorn_repeat;
-  mp.mixes = b->mixes;
-  mp.scale = a->scale;
-  mp.base = a->base;
-  mp.post_mult = c.post_mult;
-  mp.eps = c.hc_eps;
-  mp.post_out = a->post_out;
-  mp.comb_out = a->comb_out;
-  cudaStream_t mix_stream = sync_mixes ? stream : b->side;
-  if (!sync_mixes) {
-    e = cudaEventRecord(b->main_ready, stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(b->side, b->main_ready, 0);
+  if (separate) {
+    MixesParams mp = {};
+    mp.m = a->m;
+    mp.repeat = c.sinkhorn_repeat;
+    mp.mixes = b->mixes;
+    mp.scale = a->scale;
+    mp.base = a->base;
+    mp.post_mult = c.post_mult;
+    mp.eps = c.hc_eps;
+    mp.post_out = a->post_out;
+    mp.comb_out = a->comb_out;
+    cudaStream_t mix_stream = on_side ? b->side : stream;
+    if (on_side) {
+      e = cudaEventRecord(b->main_ready, stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(b->side, b->main_ready, 0);
+    }
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], mix_stream);
+    if (e == cudaSuccess) e = launch_mixes(mp, mix_stream);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[5], mix_stream);
+    if (e == cudaSuccess && on_side) e = cudaEventRecord(b->side_done, mix_stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
+  } else if (ev) {
+    // no separate mixes kernel: its profiled time is zero
+    cudaEventRecord(ev[4], stream);
+    cudaEventRecord(ev[5], stream);
   }
-  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], mix_stream);
-  if (e == cudaSuccess) e = launch_mixes(mp, mix_stream);
-  if (e == cudaSuccess && ev) e = cudaEventRecord(ev[5], mix_stream);
-  if (e == cudaSuccess) e = cudaEventRecord(b->side_done, mix_stream);
-  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
   if (ev) ++b->prof_calls;
-  b->side_pending = true;
-  b->side_capture = capture;
+  if (on_side) {
+    b->side_pending = true;
+    b->side_capture = capture;
+  }
   b->last_error.clear();
   return MHC_OK;
 }
@@ -299,6 +328,7 @@ void release(mhc_boundary *b) {
   if (b->staging) cudaFree(b->staging);
   if (b->mixes) cudaFree(b->mixes);
   if (b->part) cudaFree(b->part);
+  if (b->fold) cudaFree(b->fold);
   if (b->err) cudaFree(b->err);
   if (b->main_ready) cudaEventDestroy(b->main_ready);
   if (b->side_done) cudaEventDestroy(b->side_done);
@@ -323,12 +353,9 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   if (c.sinkhorn_repeat < 1 || c.sinkhorn_repeat > 10000)
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "sinkhorn_repeat must be in [1, 10000]");
   if (c.top_k < 0 || c.top_k > 64) return fail(g_create_error, MHC_ERR_INVALID_ARG, "top_k must be in [0, 64]");
-  if (c.top_k > 0 && stage_smem_bytes(32, true, c.tp, c.top_k) > STAGE_SMEM_LIMIT)
-    return fail(g_create_error, MHC_ERR_UNSUPPORTED, "tp * top_k = %d route slots exceed the stage kernel's shared memory",
-                c.tp * c.top_k);
   if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
-  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING))
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING | MHC_FLAG_SIDE_MIXES))
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "unknown flag bits 0x%x", c.flags);
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count)
@@ -355,6 +382,7 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   }
   e = cudaMalloc(&b->mixes, cap * MIX * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&b->part, cap * part_row_floats(b->slices) * sizeof(float));
+  if (e == cudaSuccess && c.top_k > 0) e = cudaMalloc(&b->fold, cap * size_t(c.hidden) * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->err, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(b->err, 0, sizeof(unsigned int));
   if (e == cudaSuccess && (c.flags & MHC_FLAG_HOST_STAGING)) {
@@ -463,7 +491,7 @@ mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *host
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "host to device copy: %s", cudaGetErrorString(e));
   s = launch_call(b, &d, nullptr, stream);
   if (s != MHC_OK) return s;
-  if (!(c.flags & MHC_FLAG_SYNC_MIXES)) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+  if (b->side_pending) e = cudaStreamWaitEvent(stream, b->side_done, 0);
   const Copy out[] = {
       {host->residual_out, d.residual_out, M * HC * H * 2},
       {host->layer_input, d.layer_input, M * H * 2},
@@ -510,7 +538,10 @@ mhc_status_t mhc_boundary_destroy(mhc_boundary_t *b) {
 
 size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden) { return scale_bytes(m, hidden); }
 
-int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) { return b ? 3 : 0; }
+int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) {
+  if (!b) return 0;
+  return (b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 3 : 2;
+}
 
 mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls) {
   if (!b) return MHC_ERR_INVALID_ARG;

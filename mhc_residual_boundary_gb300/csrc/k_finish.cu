@@ -1,9 +1,9 @@
 // k_finish.cu -- finish kernel of the mHC boundary.  Per token:
 //
-//  1. sums the stage kernel's per-slice partials in slice order (24 GEMV
+//  1. sums the stage kernel's per-group partials in group order (24 GEMV
 //     outputs and the sum of squares of the new streams);
-//  2. rstd = 1/sqrt(ss / (4H) + rms_eps), mixes = raw * rstd (kept for the
-//     side kernel), pre_j = sigmoid(mixes_j * scale[0] + base[j]) + hc_eps
+//  2. rstd = 1/sqrt(ss / (4H) + rms_eps), mixes = raw * rstd,
+//     pre_j = sigmoid(mixes_j * scale[0] + base[j]) + hc_eps
 //     ([GLM] _BoundaryDeviceKernel.kernel, "rstd", "pre_mix");
 //  3. collapse c = bf16(sum_j new_j * pre_j), inv_rms = 1/sqrt(sum c^2 / H +
 //     norm_eps), out = bf16((c * inv_rms) * gamma) ([GLM] "collapse",
@@ -12,18 +12,24 @@
 //     amax * (1/448) rounded up to a power of two, E4M3 values of
 //     out * 2^(127 - e) with hardware nearest-even satfinite conversions,
 //     scales at the 128x4 swizzled offset, padding-row scales zeroed ([DSV]
-//     _LamportMHCDeviceKernel.kernel, quantize branch).
+//     _LamportMHCDeviceKernel.kernel, quantize branch);
+//  5. with `post_out` set, the next boundary's post-mix and Sinkhorn residual
+//     mix as well ([GLM] _MixesDeviceKernel.kernel and _sinkhorn): the mixes
+//     warp keeps the normalised mixes of up to 32 of the CTA's tokens and
+//     runs their Sinkhorn chains one token per lane, while the other seven
+//     warps collapse the batch's last token; otherwise the raw mixes go to
+//     `mixes` for the side kernel.
 //
 // Layout on the GPU: persistent CTAs of 256 threads, two per SM where the
 // shared memory allows, each taking tokens blockIdx.x, blockIdx.x + gridDim.x,
 // ...  A token's four new streams are one contiguous 8H-byte run of
 // residual_out and its partial sums one 16-byte-padded row, so each token
 // arrives in shared memory by two bulk copies into a two-slot ring; thread 0
-// refills a slot as soon as the token in it has been collapsed, so the next
-// token's copies are in flight while this one is normalised and stored, and
-// the two CTAs of an SM interleave their per-token barriers.  gamma is held in
-// registers for the whole kernel.  Every wait is bounded; a
-// wait that gives up sets bit 1 of the error word.
+// refills a slot as soon as the token in it is done, so the next token's
+// copies are in flight while this one is normalised and stored.  The collapse
+// keeps c in the slot (over stream 0, which the same thread has just read), so
+// the fragment loops are plain runtime loops.  Every wait is bounded; a wait
+// that gives up sets bit 1 of the error word.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
@@ -35,12 +41,15 @@ namespace mhc {
 namespace {
 
 constexpr int NT = 256;
-constexpr int NFMAX = MAX_HIDDEN / VEC / NT;   // fragments of a stream row per thread at most
-static_assert(NFMAX == 8, "launch_finish dispatches NF = 1 .. 8");
+constexpr int CWARPS = 7;                      // collapse warps
+constexpr int CT = CWARPS * 32;                // collapse threads
+constexpr int MIX_WARP = CWARPS;               // the mixes warp
 constexpr int MAX_SLOTS = 2;
+constexpr int BATCH = 32;                      // tokens per lane-parallel Sinkhorn batch
 constexpr size_t SMEM_BUDGET = 110 * 1024;     // ring bytes of one CTA: two CTAs fit an SM
-constexpr size_t SMEM_LIMIT = 200 * 1024;      // one slot at H = 16384 is 153 KB
+constexpr size_t SMEM_LIMIT = 200 * 1024;      // one slot at H = 16384 is 133 KB
 constexpr uint32_t WAIT_LIMIT = 1u << 22;      // polls before a wait gives up
+static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collapse threads");
 
 // Bytes of one ring slot: the token's four stream rows, then its partial-sum row.
 __host__ __device__ inline size_t slot_bytes(int hidden, int part_stride) {
@@ -84,13 +93,71 @@ __device__ __forceinline__ size_t swizzle_128x4(int row, int col, int cols) {
   return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (col % 4);
 }
 
-// NF: 16-byte fragments of a stream row per thread (ceil(H / 8 / 256)).
-template <int NF>
+// Next boundary's post-mix and Sinkhorn residual mix of one token, from its
+// normalised mixes, in one thread ([GLM] _MixesDeviceKernel):
+//   post_j = sigmoid(mixes_{4+j} * scale[1] + base[4+j]) * post_mult
+//   logits c[r][k] = mixes_{8+4r+k} * scale[2] + base[8+4r+k]
+//   rows: c = exp(c - max_k c) / sum_k + eps
+//   `repeat` rounds: (from the second round) rows c /= (row sum + eps);
+//                    columns c /= (column sum + eps)
+// with the four-term sums paired ((a + b) + (c + d)) and reciprocals
+// multiplied in.  The reciprocals are CUDA's fast approximate division
+// (within 2 ulp of 1/x for these positive sums), the same operations as the
+// side-stream kernel, so both give the same bits.
+__device__ __forceinline__ float rcp_fast(float x) { return __fdividef(1.0f, x); }
+__device__ __forceinline__ float sum4(float a, float b, float c, float d) {
+  return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+}
+
+__device__ __noinline__ void post_and_sinkhorn(const FinishParams &p, int t, const float *mix) {
+#pragma unroll
+  for (int j = 0; j < HC; ++j) {
+    const float z = __fadd_rn(__fmul_rn(mix[HC + j], p.scale[1]), p.base[HC + j]);
+    p.post_out[(size_t)t * HC + j] = __fmul_rn(sigmoid(z), p.post_mult);
+  }
+  const float eps = p.hc_eps, s2 = p.scale[2];
+  float c[HC * HC];
+#pragma unroll
+  for (int i = 0; i < HC * HC; ++i) c[i] = __fadd_rn(__fmul_rn(mix[2 * HC + i], s2), p.base[2 * HC + i]);
+#pragma unroll
+  for (int r = 0; r < HC; ++r) {
+    float *x = c + HC * r;
+    const float peak = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) x[k] = expf(__fsub_rn(x[k], peak));
+    const float inv = rcp_fast(sum4(x[0], x[1], x[2], x[3]));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) x[k] = __fadd_rn(__fmul_rn(x[k], inv), eps);
+  }
+#pragma unroll 1
+  for (int it = 0; it < p.repeat; ++it) {
+    if (it > 0) {
+#pragma unroll
+      for (int r = 0; r < HC; ++r) {
+        float *x = c + HC * r;
+        const float inv = rcp_fast(__fadd_rn(sum4(x[0], x[1], x[2], x[3]), eps));
+#pragma unroll
+        for (int k = 0; k < HC; ++k) x[k] = __fmul_rn(x[k], inv);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < HC; ++k) {
+      const float inv = rcp_fast(__fadd_rn(sum4(c[k], c[HC + k], c[2 * HC + k], c[3 * HC + k]), eps));
+#pragma unroll
+      for (int r = 0; r < HC; ++r) c[HC * r + k] = __fmul_rn(c[HC * r + k], inv);
+    }
+  }
+  float *dst = p.comb_out + (size_t)t * HC * HC;
+#pragma unroll
+  for (int i = 0; i < HC * HC; ++i) dst[i] = c[i];
+}
+
 __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[MAX_SLOTS];
   __shared__ float tot_s[VALUES];
-  __shared__ float red_s[NT / 32];
+  __shared__ float red_s[CWARPS];
+  __shared__ float mix_s[BATCH][MIX];
   __shared__ int abort_s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = p.hidden;
@@ -123,115 +190,115 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
     for (; filled < slots && filled < n_tok; ++filled) fill(filled);
 
   const int cols = H / 32;
-  uint4 gam[NF];   // this thread's fragments of gamma, the same for every token
-#pragma unroll
-  for (int i = 0; i < NF; ++i) {
-    const int fr = tid + i * NT;
-    gam[i] = fr < nfrag ? ld_vec(p.gamma + (size_t)fr * VEC) : make_uint4(0u, 0u, 0u, 0u);
-  }
   for (int k = 0; k < n_tok; ++k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
-    const unsigned char *slot = smem + size_t(k % slots) * sbytes;
+    unsigned char *slot = smem + size_t(k % slots) * sbytes;
     if (!tc::mbar_wait_bounded(&full[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) abort_s = 1;
-    const uint16_t *sv = reinterpret_cast<const uint16_t *>(slot);
     const float *part_s = reinterpret_cast<const float *>(slot + stream_bytes);
 
-    // 1. partial sums over the slices, in slice order within each lane
+    // 1. partial sums over the groups, in group order within each lane
     for (int v = warp; v < VALUES; v += NT / 32) {
       float s = 0.f;
-      for (int sl = lane; sl < p.slices; sl += 32) s += part_s[sl * VALUES + v];
+      for (int g = lane; g < p.slices; g += 32) s += part_s[g * VALUES + v];
       s = warp_sum(s);
       if (lane == 0) tot_s[v] = s;
     }
     __syncthreads();
     if (abort_s) break;
-
-    // 2. mixes (for the side kernel) and pre, the latter on every thread
     const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(tot_s[MIX], float(HC * H)), p.rms_eps)));
-    if (tid < MIX) {
-      const float mix = __fmul_rn(tot_s[tid], rstd);
-      p.mixes[(size_t)t * MIX + tid] = mix;
-      if (p.mixes_out) p.mixes_out[(size_t)t * MIX + tid] = mix;
-    }
-    float pre[HC];
-#pragma unroll
-    for (int j = 0; j < HC; ++j) {
-      const float z = __fadd_rn(__fmul_rn(__fmul_rn(tot_s[j], rstd), p.scale[0]), p.base[j]);
-      pre[j] = __fadd_rn(sigmoid(z), p.hc_eps);
-    }
-    if (p.pre_out && tid < HC)
-      p.pre_out[(size_t)t * HC + tid] = tid == 0 ? pre[0] : tid == 1 ? pre[1] : tid == 2 ? pre[2] : pre[3];
 
-    // 3. collapse, kept in registers as BF16 for the normalisation
-    const float p0 = pre[0], p1 = pre[1], p2 = pre[2], p3 = pre[3];
-    uint4 cfr[NF];
-    float ssq = 0.f;
+    if (warp == MIX_WARP) {
+      // 2. mixes and pre of this token; (fused) post + Sinkhorn per batch of
+      // tokens, one token per lane, beside the batch's last collapse
+      const int b = k % BATCH;
+      if (lane < MIX) {
+        const float mix = __fmul_rn(tot_s[lane], rstd);
+        mix_s[b][lane] = mix;
+        if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
+        if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
+        if (p.pre_out && lane < HC)
+          p.pre_out[(size_t)t * HC + lane] =
+              __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+      }
+      __syncwarp();
+      if (p.post_out && (b == BATCH - 1 || k == n_tok - 1)) {
+        if (lane <= b) post_and_sinkhorn(p, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
+        __syncwarp();
+      }
+    } else {
+      // 3. collapse into the slot (c over stream 0), sum of squares of c
+      float pre[HC];
 #pragma unroll
-    for (int i = 0; i < NF; ++i) {
-      const int fr = tid + i * NT;
-      cfr[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (fr < nfrag) {
+      for (int j = 0; j < HC; ++j) {
+        const float z = __fadd_rn(__fmul_rn(__fmul_rn(tot_s[j], rstd), p.scale[0]), p.base[j]);
+        pre[j] = __fadd_rn(sigmoid(z), p.hc_eps);
+      }
+      uint16_t *sv = reinterpret_cast<uint16_t *>(slot);
+      float ssq = 0.f;
+#pragma unroll 1
+      for (int fr = tid; fr < nfrag; fr += CT) {
         float n0[8], n1[8], n2[8], n3[8], c[8];
-        const uint16_t *s = sv + (size_t)fr * VEC;
+        uint16_t *s = sv + (size_t)fr * VEC;
         unpack8(*reinterpret_cast<const uint4 *>(s), n0);
         unpack8(*reinterpret_cast<const uint4 *>(s + H), n1);
         unpack8(*reinterpret_cast<const uint4 *>(s + 2 * H), n2);
         unpack8(*reinterpret_cast<const uint4 *>(s + 3 * H), n3);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], p0), __fmul_rn(n1[e], p1)),
-                           __fadd_rn(__fmul_rn(n2[e], p2), __fmul_rn(n3[e], p3)));
-        cfr[i] = round8(c);
+          c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], pre[0]), __fmul_rn(n1[e], pre[1])),
+                           __fadd_rn(__fmul_rn(n2[e], pre[2]), __fmul_rn(n3[e], pre[3])));
+        *reinterpret_cast<uint4 *>(s) = round8(c);
 #pragma unroll
         for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
       }
-    }
-    ssq = warp_sum(ssq);
-    if (lane == 0) red_s[warp] = ssq;
-    // the slot's next fill is an async-proxy write after these generic reads
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    // the slot has been read: it takes the token `slots` places further on
-    if (tid == 0 && filled < n_tok) fill(filled++);
-    float sq = 0.f;
+      ssq = warp_sum(ssq);
+      if (lane == 0) red_s[warp] = ssq;
+      asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
+      float sq = 0.f;
 #pragma unroll
-    for (int w = 0; w < NT / 32; ++w) sq += red_s[w];
-    const float ir = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(sq, float(H)), p.norm_eps)));
+      for (int w = 0; w < CWARPS; ++w) sq += red_s[w];
+      const float ir = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(sq, float(H)), p.norm_eps)));
 
-    // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
-#pragma unroll
-    for (int i = 0; i < NF; ++i) {
-      const int fr = tid + i * NT;
-      const bool live = fr < nfrag;
-      float o[8];
-      if (live) {
-        float c[8], g[8];
-        unpack8(cfr[i], c);
-        unpack8(gam[i], g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(c[e], ir), g[e]);
-        st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, round8(o));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = 0.f;
-      }
-      if (p.mx_values) {
-        float amax = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const uint32_t e8 = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
-        const float inv = inv_scale(e8);
+      // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
+#pragma unroll 1
+      for (int base = 0; base < nfrag; base += CT) {
+        const int fr = base + tid;
+        const bool live = fr < nfrag;
+        float o[8];
         if (live) {
-          uint2 q;
-          q.x = e4m3x4(__fmul_rn(o[0], inv), __fmul_rn(o[1], inv), __fmul_rn(o[2], inv), __fmul_rn(o[3], inv));
-          q.y = e4m3x4(__fmul_rn(o[4], inv), __fmul_rn(o[5], inv), __fmul_rn(o[6], inv), __fmul_rn(o[7], inv));
-          *reinterpret_cast<uint2 *>(p.mx_values + (size_t)t * H + (size_t)fr * VEC) = q;
-          if ((fr & 3) == 0) p.mx_scales[swizzle_128x4(t, fr / 4, cols)] = uint8_t(e8);
+          float c[8], g[8];
+          unpack8(*reinterpret_cast<const uint4 *>(sv + (size_t)fr * VEC), c);
+          unpack8(ld_vec(p.gamma + (size_t)fr * VEC), g);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(c[e], ir), g[e]);
+          st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, round8(o));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] = 0.f;
+        }
+        if (p.mx_values) {
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+          const uint32_t e8 = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
+          const float inv = inv_scale(e8);
+          if (live) {
+            uint2 q;
+            q.x = e4m3x4(__fmul_rn(o[0], inv), __fmul_rn(o[1], inv), __fmul_rn(o[2], inv), __fmul_rn(o[3], inv));
+            q.y = e4m3x4(__fmul_rn(o[4], inv), __fmul_rn(o[5], inv), __fmul_rn(o[6], inv), __fmul_rn(o[7], inv));
+            *reinterpret_cast<uint2 *>(p.mx_values + (size_t)t * H + (size_t)fr * VEC) = q;
+            if ((fr & 3) == 0) p.mx_scales[swizzle_128x4(t, fr / 4, cols)] = uint8_t(e8);
+          }
         }
       }
     }
+    // the slot's next fill is an async-proxy write after these generic accesses
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    // the slot is done: it takes the token `slots` places further on
+    if (tid == 0 && filled < n_tok) fill(filled++);
   }
   pdl_launch_dependents();
 
@@ -252,22 +319,13 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
 
 }  // namespace
 
-using FinishKernel = void (*)(FinishParams, int);
-constexpr FinishKernel kFinish[NFMAX] = {k_finish<1>, k_finish<2>, k_finish<3>, k_finish<4>,
-                                         k_finish<5>, k_finish<6>, k_finish<7>, k_finish<8>};
-
 cudaError_t finish_set_attributes() {
-  for (FinishKernel k : kFinish) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return cudaFuncSetAttribute(k_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
 }
 
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl) {
-  const int nf = (p.hidden / VEC + NT - 1) / NT;
-  if (nf < 1 || nf > NFMAX || p.part_stride % 4 || p.part_stride < p.slices * VALUES) return cudaErrorInvalidValue;
+  if (p.hidden % VEC || p.hidden > MAX_HIDDEN || p.part_stride % 4 || p.part_stride < p.slices * VALUES)
+    return cudaErrorInvalidValue;
   const int slots = ring_slots(p.hidden, p.part_stride);
   const size_t smem = size_t(slots) * slot_bytes(p.hidden, p.part_stride);
   if (smem > SMEM_LIMIT) return cudaErrorInvalidValue;
@@ -284,7 +342,7 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kFinish[nf - 1], p, slots);
+  return cudaLaunchKernelEx(&cfg, k_finish, p, slots);
 }
 
 }  // namespace mhc

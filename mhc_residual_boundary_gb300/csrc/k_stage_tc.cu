@@ -1,27 +1,25 @@
 // k_stage_tc.cu -- stage kernel: TMA-fed load pipeline, post-mix on CUDA
 // cores, prenorm GEMV on tcgen05 tensor cores.
 //
-// Work unit: 32 tokens x one group of 128 hidden columns, so that every row
-// piece a unit reads is a 256-byte run (HBM serves these about 10% faster
-// than 128-byte pieces of rows 12 KB apart).  Units are numbered group-major
-// and every CTA (one per SM, persistent) takes a contiguous range of them, so
-// a CTA stages each group's hc_fn once.  Per CTA (8 warps):
+// Work unit: 32 tokens x one group of 128 hidden columns (every row piece a
+// unit reads is a 256-byte run).  Units are numbered group-major and every
+// CTA (one per SM, persistent) takes a contiguous range of them, so a CTA
+// stages each group's hc_fn once.  Roles in a CTA of 17 warps:
 //
-//   loads: stage q (tokens 8q .. 8q+7) of every unit goes to ring slot q by
-//     four TMA tensor copies -- the partials [tp][m][H] (one 3-D box: 128
-//     columns x 8 tokens x tp ranks), the residual streams [m][4][H], post
-//     [m][4] and comb [m][4][4] -- tracked by the slot's mbarrier transaction
-//     count.  Out-of-range tokens and columns arrive as zeros.  Lane 0 of
-//     warp q issues them: the next unit's copies as soon as warps q and q + 4
-//     have moved the current stage to registers.
-//   mixing: warps q and q + 4 own slot q.  A thread handles two (token,
-//     16-byte fragment) items of its stage: stage-1 sum of the tp partials in
-//     FP32 in rank order, rounded to BF16 ([DSV]
-//     _LamportMHCDeviceKernel.kernel, lane_sum); post-mix of the four streams
-//     ([GLM] _BoundaryDeviceKernel.kernel, "mixed"), stored to residual_out
-//     and, as the MMA's A operand, to shared memory; the sum of squares of
-//     the new streams, reduced over the token's 16 lanes and written to the
-//     partial-sum scratch.
+//   control warp: an event loop that never blocks (one lane issues).  It refills ring
+//     slots as soon as the mixer warps release them -- stage q (tokens
+//     8q .. 8q+7) of every unit by four TMA tensor copies: the partials
+//     [tp][m][H] (one 3-D box of 128 columns x 8 tokens x tp ranks), the
+//     residual streams [m][4][H], post [m][4] and comb [m][4][4], counted on
+//     the slot's mbarrier; out-of-range tokens and columns arrive as zeros --
+//     and it issues a unit's MMAs as soon as its A operand is complete.
+//   16 mixer warps: four per stage, one (token, 16-byte fragment) item per
+//     thread.  Stage-1 sum of the tp partials in FP32 in rank order, rounded
+//     to BF16 ([DSV] _LamportMHCDeviceKernel.kernel, lane_sum); post-mix of
+//     the four streams ([GLM] _BoundaryDeviceKernel.kernel, "mixed"), stored
+//     to residual_out and, as the MMA's A operand, to shared memory; the sum
+//     of squares of the new streams over the token's 16 lanes.  They also
+//     build the B operand when the group changes and read the accumulators.
 //   GEMV (tensor cores): the MMA's 128 rows are (token t, stream j) with
 //     row = 4t + j, its K the unit's 128 columns and its 96 columns (stream
 //     j', output i): D[(t,j)][(j',i)] = sum_h new_j[t][h] * fn[j'*H + h][i];
@@ -29,16 +27,20 @@
 //     ([GLM] _BoundaryDeviceKernel.kernel, "partial").  hc_fn is FP32; it is
 //     split into three BF16 terms (hi + mid + lo, remainder below 2^-24
 //     relative) so that each BF16 x BF16 product is exact and the sum
-//     accumulates in FP32 in tensor memory: 3 x 8 MMAs of M=128, N=96, K=16,
-//     issued by one thread into one of two accumulators (by unit parity).
+//     accumulates in FP32 in tensor memory: 3 x 8 MMAs of M=128, N=96, K=16
+//     into one of two accumulators (by unit parity).
 //   epilogue (one unit later, so that it overlaps the next unit's loads):
-//     TMEM lane quarter q holds the rows of stage q's tokens, four lanes per
-//     token; warp q reads outputs 0-11 and warp q + 4 outputs 12-23 of all
-//     four blocks, the four streams of a token are added in the order
-//     ((j0 + j1) + (j2 + j3)) with warp shuffles, and the sums go to the
-//     scratch rows [m][groups][25] (24 sums + the sum of squares; rows padded
-//     to 16 bytes) that the finish kernel reduces.
-// Every wait is bounded; a wait that gives up sets bit 1 of the error word.
+//     warp w reads TMEM lane quarter w % 4 (the rows of stage w % 4's
+//     tokens, four lanes per token) and six of the 24 outputs of all four
+//     stream blocks; each lane keeps its own stream's block and the four
+//     lanes of a token add them in the order ((j0 + j1) + (j2 + j3)).  The
+//     sums go to the scratch rows [m][groups][25] (24 sums + the sum of
+//     squares; rows padded to 16 bytes) that the finish kernel reduces.
+//
+// The mixers build the first group's B while the control warp starts the
+// pipeline, and the later groups' hc_fn rows are prefetched into L2, so a
+// later B build does not wait on DRAM.  Every wait is bounded; a wait that gives up sets bit 1 of the error
+// word and stops the CTA.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
@@ -54,111 +56,195 @@
 namespace mhc {
 namespace {
 
-constexpr int NT = 256;                       // 8 warps (256 threads leave 255 registers a thread)
+constexpr int MIX_WARPS = 16;                 // mixer warps
+constexpr int CTRL_WARP = MIX_WARPS;          // the control warp's index
+constexpr int NT = (MIX_WARPS + 1) * 32;      // 544 threads
+constexpr int MIX_THREADS = MIX_WARPS * 32;
 constexpr int UT = 32;                        // tokens per unit
 constexpr int ROWS = HC * UT;                 // MMA M: (token, stream) rows
 constexpr int UK = TC_GROUP_COLS;             // MMA K per term: the unit's 128 columns
 constexpr int KCOLS = UK / 8;                 // core-matrix columns of 8 BF16
 constexpr int UN = HC * MIX;                  // MMA N: (stream', output) columns
 constexpr int QT = 8;                         // tokens per pipeline stage
-constexpr int NSTAGE = UT / QT;               // ring slots = stages per unit
-constexpr int SLOT_THREADS = 64;              // threads per slot (two warps)
+constexpr int NSTAGE = UT / QT;               // stages per unit
+constexpr int STAGE_WARPS = MIX_WARPS / NSTAGE;   // mixer warps per stage
 constexpr int FRAGS = UK / VEC;               // 16-byte fragments per row piece
-constexpr int A_KCOL = ROWS * 16 + 16;        // bytes between A core columns (+16: no bank conflicts)
+constexpr int A_KCOL = ROWS * 16 + 16;        // bytes between A core columns (+16: fewer bank conflicts)
 constexpr int A_BYTES = KCOLS * A_KCOL;
 constexpr int B_KCOL = UN * 16;               // bytes between B core columns
 constexpr int B_BYTES = 3 * KCOLS * B_KCOL;   // hi, mid, lo
 constexpr int ROW = UK * 2;                   // bytes of one 128-column BF16 row piece
-constexpr int STAGE_PART = 0;                 // [tp][8 tokens][128] bf16
-constexpr int STAGE_RES = TP_TMA_MAX * QT * ROW;          // [8 tokens][4][128] bf16
-constexpr int STAGE_POST = STAGE_RES + QT * HC * ROW;     // [8][4] f32
-constexpr int STAGE_COMB = STAGE_POST + 128;              // [8][16] f32
-constexpr int STAGE_BYTES = STAGE_COMB + QT * HC * HC * 4;
-constexpr int OUT_HALF = MIX / 2;             // outputs one epilogue warp reads per block
+constexpr int MAX_SLOTS = 8;
 constexpr uint32_t D_STRIDE = 128;            // TMEM columns between the two accumulators
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;     // polls before a wait gives up
-static_assert(QT * HC * 4 <= 128, "post block");
-static_assert(UK % 16 == 0 && UN % 16 == 0 && UN <= 256, "MMA shape");
-static_assert(QT * FRAGS == 2 * SLOT_THREADS, "two items per thread");
+constexpr int SMEM_MAX = 227 * 1024;          // dynamic shared memory of one CTA
+constexpr int B_PAIRS = (UK / 2) * UN / MIX_THREADS;   // hc_fn element pairs per mixer thread
+constexpr int OUTS = MIX / STAGE_WARPS;       // outputs one epilogue warp reads per block (6)
+static_assert(QT * FRAGS == STAGE_WARPS * 32, "one item per mixer thread");
 static_assert(ROWS == 4 * 32 && QT * HC == 32, "one TMEM lane quarter per stage");
-static_assert(OUT_HALF % 4 == 0 && OUT_HALF == 3 * HC, "epilogue split");
+static_assert((UK / 2) * UN % MIX_THREADS == 0 && B_PAIRS == 12, "B build split");
+static_assert(OUTS == 6, "epilogue split: four outputs plus two");
+static_assert(UK % 16 == 0 && UN % 16 == 0 && UN <= 256, "MMA shape");
 
+// Shared memory: control block, A, B, then the ring of stage slots.
 struct Layout {
-  static constexpr size_t a = 0;
-  static constexpr size_t b = A_BYTES;
-  static constexpr size_t stages = ((b + B_BYTES + 127) / 128) * 128;
-  static constexpr size_t full = stages + size_t(NSTAGE) * STAGE_BYTES;  // uint64 [NSTAGE]
-  static constexpr size_t empty = full + 8 * NSTAGE;                     // uint64 [NSTAGE]
-  static constexpr size_t mma = empty + 8 * NSTAGE;                      // uint64 [2]
-  static constexpr size_t slot = mma + 16;                               // TMEM address
-  static constexpr size_t cabort = slot + 4;                             // int
-  static constexpr size_t total = cabort + 12;
-  static_assert(b % 16 == 0 && STAGE_BYTES % 128 == 0, "TMA / MMA alignment");
-  static_assert(STAGE_RES % 128 == 0 && STAGE_POST % 128 == 0 && STAGE_COMB % 128 == 0, "TMA alignment");
-  static_assert(full % 8 == 0, "mbarrier alignment");
-  static_assert(total <= 227 * 1024, "shared memory");
+  static constexpr int full = 0;                        // uint64 [MAX_SLOTS]
+  static constexpr int empty = full + 8 * MAX_SLOTS;    // uint64 [MAX_SLOTS]
+  static constexpr int afull = empty + 8 * MAX_SLOTS;   // uint64: A operand complete
+  static constexpr int mma = afull + 8;                 // uint64 [2]: MMAs of a unit done
+  static constexpr int slot = mma + 16;                 // TMEM address
+  static constexpr int abort = slot + 4;                // int
+  static constexpr int a = 256;
+  static constexpr int b = a + A_BYTES;
+  static constexpr int ring = b + B_BYTES;
+  static_assert(abort + 4 <= a, "control block");
+  static_assert(a % 128 == 0 && b % 128 == 0 && ring % 128 == 0, "TMA / MMA alignment");
 };
 
-__device__ __forceinline__ void cta_sync() { asm volatile("bar.sync 0;" ::: "memory"); }
-
-// The group's hc_fn as three BF16 B operands (hi, mid, lo), K-major core
-// matrices [term][core column][8-column block][8 columns][8 inputs];
-// column n = stream * 24 + output, input k = column in the group.  Every
-// thread issues all its loads before the first split, so the build costs
-// one memory latency rather than one per element pair.
-constexpr int B_PAIRS = (UK / 2) * UN / NT;   // element pairs per thread
-static_assert((UK / 2) * UN % NT == 0, "B build split");
-__device__ __noinline__ void build_b(const StageParams &p, int h0, unsigned char *b_s) {
-  float x0[B_PAIRS], x1[B_PAIRS];
-#pragma unroll
-  for (int it = 0; it < B_PAIRS; ++it) {
-    const int e = threadIdx.x + it * NT;
-    const int kp = e / UN, n = e % UN, j = n / MIX, i = n % MIX;
-    const int h = h0 + 2 * kp;
-    const float *src = p.hc_fn + ((size_t)j * p.hidden + h) * MIX + i;
-    x0[it] = h < p.hidden ? __ldg(src) : 0.f;
-    x1[it] = h + 1 < p.hidden ? __ldg(src + MIX) : 0.f;
-  }
-#pragma unroll
-  for (int it = 0; it < B_PAIRS; ++it) {
-    const int e = threadIdx.x + it * NT;
-    const int kp = e / UN, n = e % UN, k = 2 * kp;
-    const uint32_t hi = pack_bf16x2(x0[it], x1[it]);
-    const float r0 = __fsub_rn(x0[it], bf16_lo(hi)), r1 = __fsub_rn(x1[it], bf16_hi(hi));
-    const uint32_t mid = pack_bf16x2(r0, r1);
-    const uint32_t lo = pack_bf16x2(__fsub_rn(r0, bf16_lo(mid)), __fsub_rn(r1, bf16_hi(mid)));
-    const size_t inner = size_t(n / 8) * 128 + (n % 8) * 16 + (k % 8) * 2;
-    *reinterpret_cast<uint32_t *>(b_s + size_t(0 * KCOLS + k / 8) * B_KCOL + inner) = hi;
-    *reinterpret_cast<uint32_t *>(b_s + size_t(1 * KCOLS + k / 8) * B_KCOL + inner) = mid;
-    *reinterpret_cast<uint32_t *>(b_s + size_t(2 * KCOLS + k / 8) * B_KCOL + inner) = lo;
-  }
+// A stage slot: partials [tp][8][128] bf16, streams [8][4][128] bf16,
+// post [8][4] f32, comb [8][16] f32 (each part 128-byte aligned).
+__host__ __device__ constexpr int slot_res(int tp) { return tp * QT * ROW; }
+__host__ __device__ constexpr int slot_post(int tp) { return slot_res(tp) + QT * HC * ROW; }
+__host__ __device__ constexpr int slot_comb(int tp) { return slot_post(tp) + QT * HC * 4; }
+__host__ __device__ constexpr int slot_bytes(int tp) { return slot_comb(tp) + QT * HC * HC * 4; }
+__host__ __device__ constexpr int ring_slots(int tp) {
+  return (SMEM_MAX - Layout::ring) / slot_bytes(tp) < MAX_SLOTS ? (SMEM_MAX - Layout::ring) / slot_bytes(tp)
+                                                                 : MAX_SLOTS;
 }
+static_assert(slot_bytes(1) % 128 == 0 && slot_post(1) % 128 == 0 && slot_comb(1) % 128 == 0, "slot alignment");
+static_assert(ring_slots(TP_TMA_MAX) >= NSTAGE, "a unit's four stages fit the ring");
 
-// Two BF16 values of a packed word as an FP32 pair.
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-__device__ __forceinline__ void unpack4x2(const uint4 &v, float2 (&x)[4]) {
-  x[0] = unpack2(v.x);
-  x[1] = unpack2(v.y);
-  x[2] = unpack2(v.z);
-  x[3] = unpack2(v.w);
-}
-// Rounds four FP32 pairs to BF16 in place; returns the packed words.
-__device__ __forceinline__ uint4 round4x2(float2 (&x)[4]) {
-  const uint4 w = make_uint4(pack_bf16x2(x[0].x, x[0].y), pack_bf16x2(x[1].x, x[1].y),
-                             pack_bf16x2(x[2].x, x[2].y), pack_bf16x2(x[3].x, x[3].y));
-  unpack4x2(w, x);
-  return w;
-}
 __device__ __forceinline__ float lane4(const float4 &v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
 
-// One (token, fragment) of a filled stage, copied to registers so that the
-// ring slot can be released before the arithmetic.
+// Rounds four FP32 pairs to BF16 in place; returns the packed words.
+__device__ __forceinline__ uint4 round4x2(float2 (&x)[4]) {
+  const uint4 w = make_uint4(pack_bf16x2(x[0].x, x[0].y), pack_bf16x2(x[1].x, x[1].y),
+                             pack_bf16x2(x[2].x, x[2].y), pack_bf16x2(x[3].x, x[3].y));
+  x[0] = unpack2(w.x);
+  x[1] = unpack2(w.y);
+  x[2] = unpack2(w.z);
+  x[3] = unpack2(w.w);
+  return w;
+}
+
+// FP32 pair += the BF16 pair of a packed word; the widening is folded into
+// the add (exact, so each lane rounds once, as the FP32 add of the widened
+// value would).
+__device__ __forceinline__ void add_bf16x2(float2 &acc, uint32_t w) {
+  asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w));
+}
+
+// ------------------------------------------------------------- B operand
+// The group's hc_fn as three BF16 B operands (hi, mid, lo), K-major core
+// matrices [term][core column][8-column block][8 columns][8 inputs];
+// column n = stream * 24 + output, input k = column in the group.  Mixer
+// thread `tid` owns element pairs e = tid + 512 * it (inputs 2kp, 2kp + 1 of
+// column n), with (kp, n) chosen so that a warp's 32 stores fill 32 banks.
+__device__ __forceinline__ void b_pair(int e, int &kp, int &n) {
+  const int rest = e >> 5;
+  kp = (rest / 12) * 4 + (e & 3);
+  n = (rest % 12) * 8 + ((e >> 2) & 7);
+}
+
+__device__ __forceinline__ void load_b(const StageParams &p, int h0, float (&x0)[B_PAIRS], float (&x1)[B_PAIRS]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int it = 0; it < B_PAIRS; ++it) {
+    int kp, n;
+    b_pair(tid + it * MIX_THREADS, kp, n);
+    const int j = n / MIX, i = n % MIX, h = h0 + 2 * kp;
+    const float *src = p.hc_fn + ((size_t)j * p.hidden + h) * MIX + i;
+    x0[it] = h < p.hidden ? __ldg(src) : 0.f;
+    x1[it] = h + 1 < p.hidden ? __ldg(src + MIX) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_b(unsigned char *b_s, const float (&x0)[B_PAIRS], const float (&x1)[B_PAIRS]) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int it = 0; it < B_PAIRS; ++it) {
+    int kp, n;
+    b_pair(tid + it * MIX_THREADS, kp, n);
+    const uint32_t hi = pack_bf16x2(x0[it], x1[it]);
+    const float r0 = __fsub_rn(x0[it], bf16_lo(hi)), r1 = __fsub_rn(x1[it], bf16_hi(hi));
+    const uint32_t mid = pack_bf16x2(r0, r1);
+    const uint32_t lo = pack_bf16x2(__fsub_rn(r0, bf16_lo(mid)), __fsub_rn(r1, bf16_hi(mid)));
+    unsigned char *dst = b_s + (kp >> 2) * B_KCOL + (n >> 3) * 128 + (n & 7) * 16 + (kp & 3) * 4;
+    *reinterpret_cast<uint32_t *>(dst) = hi;
+    *reinterpret_cast<uint32_t *>(dst + KCOLS * B_KCOL) = mid;
+    *reinterpret_cast<uint32_t *>(dst + 2 * KCOLS * B_KCOL) = lo;
+  }
+}
+
+// Loads the group's hc_fn and stores its three BF16 terms (all loads are
+// issued before the first split, so the build costs one memory latency).
+__device__ __noinline__ void build_b(const StageParams &p, int h0, unsigned char *b_s) {
+  float x0[B_PAIRS], x1[B_PAIRS];
+  load_b(p, h0, x0, x1);
+  store_b(b_s, x0, x1);
+}
+
+// ------------------------------------------------------------- epilogue
+// Unit `i`'s GEMV sums once its MMAs are done.  Warp w reads lane quarter
+// w % 4 -- row 32q + l = (token 8q + l/4, stream l%4) -- and outputs
+// 4s .. 4s+3 and 16+2s, 17+2s (s = w / 4) of all four stream blocks; each
+// lane takes its own stream's block, the four lanes of a token add them in
+// the order ((j0 + j1) + (j2 + j3)) and lane o % 4 writes output o.
+struct Epi {
+  uint32_t tmem;
+  uint64_t *mma_bar;
+  volatile int *abort_s;
+  int i, tile, group;
+};
+
+__device__ __noinline__ void epilogue(const StageParams &p, const Epi &e) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, s = warp >> 2, j = lane & 3, d = e.i & 1;
+  const bool ok = tc::mbar_wait_bounded(&e.mma_bar[d], (e.i >> 1) & 1, WAIT_LIMIT);
+  if (!ok) *e.abort_s = 1;
+  tc::fence_after_sync();
+  const uint32_t base = e.tmem + (uint32_t(32 * q) << 16) + uint32_t(d) * D_STRIDE;
+  uint32_t r4[HC][4], r2[HC][2];
+#pragma unroll
+  for (int jb = 0; jb < HC; ++jb) {
+    tc::tmem_ld4_async(base + uint32_t(jb * MIX + 4 * s), r4[jb]);
+    tc::tmem_ld2_async(base + uint32_t(jb * MIX + 16 + 2 * s), r2[jb]);
+  }
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int jb = 0; jb < HC; ++jb) {
+    tc::tmem_hold4(r4[jb]);
+    tc::tmem_hold2(r2[jb]);
+  }
+  const int t = e.tile * UT + q * QT + (lane >> 2);
+  float *dst = p.part + (size_t)t * p.part_stride + e.group * VALUES;
+#pragma unroll
+  for (int o = 0; o < OUTS; ++o) {
+    const int c = o < 4 ? o : o - 4;
+    const uint32_t v0 = o < 4 ? r4[0][c] : r2[0][c], v1 = o < 4 ? r4[1][c] : r2[1][c];
+    const uint32_t v2 = o < 4 ? r4[2][c] : r2[2][c], v3 = o < 4 ? r4[3][c] : r2[3][c];
+    const float v = __uint_as_float(j == 0 ? v0 : j == 1 ? v1 : j == 2 ? v2 : v3);
+    float sum = v + __shfl_xor_sync(0xffffffffu, v, 1);
+    sum = sum + __shfl_xor_sync(0xffffffffu, sum, 2);
+    const int out = o < 4 ? 4 * s + o : 16 + 2 * s + (o - 4);
+    if (ok && j == (o & 3) && t < p.m) dst[out] = sum;
+  }
+}
+
+// ----------------------------------------------------------------- mixing
+// One item (token tl of the stage, fragment f) of a filled slot, moved to
+// registers so that the slot can be released before the post-mix: the
+// stage-1 sum of the tp partials in rank order (still FP32), the four source
+// streams, post and comb.
 struct Item {
-  uint4 part[TP_TMA_MAX];
+  float2 y[4];
   uint4 res[HC];
   float4 post;
   float4 comb[HC];
@@ -166,289 +252,255 @@ struct Item {
 
 __device__ __forceinline__ void load_item(int tp, const unsigned char *st, int tl, int f, Item &it) {
 #pragma unroll
-  for (int q = 0; q < TP_TMA_MAX; ++q)
-    if (q < tp) it.part[q] = *reinterpret_cast<const uint4 *>(st + STAGE_PART + (q * QT + tl) * ROW + f * 16);
+  for (int e = 0; e < 4; ++e) it.y[e] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int k = 0; k < HC; ++k)
-    it.res[k] = *reinterpret_cast<const uint4 *>(st + STAGE_RES + (tl * HC + k) * ROW + f * 16);
-  it.post = *reinterpret_cast<const float4 *>(st + STAGE_POST + tl * HC * 4);
-#pragma unroll
-  for (int k = 0; k < HC; ++k)
-    it.comb[k] = *reinterpret_cast<const float4 *>(st + STAGE_COMB + (tl * HC + k) * HC * 4);
-}
-
-// Stage 1 and post-mix of two items in one instruction stream; returns the
-// stage-1 sums and the new streams as BF16 fragments and each item's sum of
-// squares.  The post-mix runs on FP32 element pairs (packed mul / fma, each
-// lane rounded to nearest as the scalar operation would be).
-__device__ __forceinline__ void mix_pair(int tp, const Item (&it)[2], uint4 (&yb)[2], uint4 (&nv)[2][HC],
-                                         float (&ss)[2]) {
-  float2 y[2][4];
-#pragma unroll
-  for (int k = 0; k < 2; ++k)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) y[k][e] = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int q = 0; q < TP_TMA_MAX; ++q) {
-    if (q < tp) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        // FP32 += BF16 with the widening folded into the add (exact, so
-        // each lane rounds once, as the FP32 add of the widened value would)
-        const uint32_t ww[4] = {it[k].part[q].x, it[k].part[q].y, it[k].part[q].z, it[k].part[q].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;}"
-              : "+f"(y[k][e].x), "+f"(y[k][e].y) : "r"(ww[e]));
-      }
+  for (int r = 0; r < TP_TMA_MAX; ++r) {
+    if (r < tp) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(st + (r * QT + tl) * ROW + f * 16);
+      add_bf16x2(it.y[0], w.x);
+      add_bf16x2(it.y[1], w.y);
+      add_bf16x2(it.y[2], w.z);
+      add_bf16x2(it.y[3], w.w);
     }
   }
+  const unsigned char *rs = st + slot_res(tp) + tl * HC * ROW + f * 16;
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    yb[k] = round4x2(y[k]);
-    float2 res[HC][4];
+  for (int k = 0; k < HC; ++k) it.res[k] = *reinterpret_cast<const uint4 *>(rs + k * ROW);
+  it.post = *reinterpret_cast<const float4 *>(st + slot_post(tp) + tl * HC * 4);
 #pragma unroll
-    for (int c = 0; c < HC; ++c) unpack4x2(it[k].res[c], res[c]);
-    float2 ss2 = make_float2(0.f, 0.f);
+  for (int k = 0; k < HC; ++k)
+    it.comb[k] = *reinterpret_cast<const float4 *>(st + slot_comb(tp) + (tl * HC + k) * HC * 4);
+}
+
+// The stage-1 sum rounded to BF16 (yb) and the post-mixed streams
+// new_j = y * post_j + sum_k res_k * comb[k][j] (one fused multiply-add per
+// source in source order, on FP32 element pairs), rounded to BF16 (nv).
+// Returns the sum of squares of the rounded streams.
+__device__ __forceinline__ float mix_item(Item &it, uint4 &yb, uint4 (&nv)[HC]) {
+  yb = round4x2(it.y);
+  float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < HC; ++j) {
-      float2 o[4];
-      const float2 pj = dup(lane4(it[k].post, j));
-      // comb[i][j] weighs source stream i in output stream j
-      const float2 c0 = dup(lane4(it[k].comb[0], j)), c1 = dup(lane4(it[k].comb[1], j));
-      const float2 c2 = dup(lane4(it[k].comb[2], j)), c3 = dup(lane4(it[k].comb[3], j));
+  for (int j = 0; j < HC; ++j) {
+    const float2 pj = dup(lane4(it.post, j));
+    // comb[k][j] weighs source stream k in output stream j
+    float2 o[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float2 v = __fmul2_rn(y[k][e], pj);
-        v = __ffma2_rn(res[0][e], c0, v);
-        v = __ffma2_rn(res[1][e], c1, v);
-        v = __ffma2_rn(res[2][e], c2, v);
-        v = __ffma2_rn(res[3][e], c3, v);
-        o[e] = v;
-      }
-      nv[k][j] = round4x2(o);
+    for (int e = 0; e < 4; ++e) o[e] = __fmul2_rn(it.y[e], pj);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ss2 = __ffma2_rn(o[e], o[e], ss2);
+    for (int k = 0; k < HC; ++k) {
+      const float2 ck = dup(lane4(it.comb[k], j));
+      const uint32_t ww[4] = {it.res[k].x, it.res[k].y, it.res[k].z, it.res[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = __ffma2_rn(unpack2(ww[e]), ck, o[e]);
     }
-    ss[k] = ss2.x + ss2.y;
+    nv[j] = round4x2(o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) ss2 = __ffma2_rn(o[e], o[e], ss2);
   }
+  return ss2.x + ss2.y;
 }
 
-// Unit i's GEMV sums, once its MMAs are done (the tensor memory holds two
-// accumulators, by unit parity).  Lane l of a warp in lane quarter q holds
-// row 32q + l = (token 8q + l/4, stream l%4); the warp reads outputs
-// 12*half .. 12*half+11 of all four stream blocks, each lane takes its own
-// stream's block from the four lanes of its token and adds them in the order
-// ((j0 + j1) + (j2 + j3)); lane j of the token writes three of the sums.
-__device__ __forceinline__ void epilogue(const StageParams &p, uint32_t tmem, uint64_t *mma_bar, int i,
-                                         int u_begin, int n_tiles, int q, int half, bool &ok) {
-  const int lane = threadIdx.x & 31;
-  const int u = u_begin + i, grpc = u / n_tiles, tile = u % n_tiles, d = i & 1;
-  if (ok && !tc::mbar_wait_bounded(&mma_bar[d], (i >> 1) & 1, WAIT_LIMIT)) ok = false;
-  tc::fence_after_sync();
-  uint32_t raw[HC][OUT_HALF];
-  const uint32_t base = tmem + (uint32_t(32 * q) << 16) + uint32_t(d) * D_STRIDE + uint32_t(OUT_HALF * half);
-#pragma unroll
-  for (int jb = 0; jb < HC; ++jb)
-#pragma unroll
-    for (int c = 0; c < OUT_HALF; c += 4) tc::tmem_ld4_async(base + uint32_t(jb * MIX + c), &raw[jb][c]);
-  tc::tmem_wait_ld();
-#pragma unroll
-  for (int jb = 0; jb < HC; ++jb)
-#pragma unroll
-    for (int c = 0; c < OUT_HALF; c += 4) tc::tmem_hold4(&raw[jb][c]);
-  const int src = lane & ~3, j = lane & 3;
-  float out[3] = {0.f, 0.f, 0.f};
-#pragma unroll
-  for (int c = 0; c < OUT_HALF; ++c) {
-    const float s0 = __shfl_sync(0xffffffffu, __uint_as_float(raw[0][c]), src + 0);
-    const float s1 = __shfl_sync(0xffffffffu, __uint_as_float(raw[1][c]), src + 1);
-    const float s2 = __shfl_sync(0xffffffffu, __uint_as_float(raw[2][c]), src + 2);
-    const float s3 = __shfl_sync(0xffffffffu, __uint_as_float(raw[3][c]), src + 3);
-    const float sum = (s0 + s1) + (s2 + s3);
-    if (c / 3 == j) out[c % 3] = sum;
-  }
-  const int t = tile * UT + q * QT + (lane >> 2);
-  if (ok && t < p.m) {
-    float *dst = p.part + (size_t)t * p.part_stride + grpc * VALUES + OUT_HALF * half + 3 * j;
-    dst[0] = out[0];
-    dst[1] = out[1];
-    dst[2] = out[2];
-  }
-}
-
+// ------------------------------------------------------------------ kernel
+// 17 warps put five on one SM sub-partition (16384 registers each), so a
+// thread may use at most 96 registers.
 __global__ void __launch_bounds__(NT, 1)
     k_stage_tc(const StageParams p, const __grid_constant__ CUtensorMap tm_part,
                const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_post,
                const __grid_constant__ CUtensorMap tm_comb) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  unsigned char *a_s = smem + Layout::a;
-  unsigned char *b_s = smem + Layout::b;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Layout::full);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Layout::empty);
+  uint64_t *afull = reinterpret_cast<uint64_t *>(smem + Layout::afull);
   uint64_t *mma_bar = reinterpret_cast<uint64_t *>(smem + Layout::mma);
   uint32_t *slot = reinterpret_cast<uint32_t *>(smem + Layout::slot);
-  // Set before a CTA barrier and read after it: every thread takes the same
-  // decision to stop.
-  volatile int *cabort_s = reinterpret_cast<volatile int *>(smem + Layout::cabort);
+  volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Layout::abort);
+  unsigned char *a_s = smem + Layout::a;
+  unsigned char *b_s = smem + Layout::b;
+  unsigned char *ring = smem + Layout::ring;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = p.slices;                               // 128-column groups
   const int n_tiles = (p.m + UT - 1) / UT;
-  const int units = n_tiles * G;
+  const int units = n_tiles * p.slices;
   const int u_begin = int((long long)blockIdx.x * units / gridDim.x);
   const int u_end = int((long long)(blockIdx.x + 1) * units / gridDim.x);
-  const int n_units = u_end - u_begin;
+  const int n_units = u_end - u_begin;             // >= 1: the grid is at most `units`
+  const int nslot = ring_slots(p.tp), sbytes = slot_bytes(p.tp);
+  const int total_fills = n_units * NSTAGE;
+  const int first_group = u_begin / n_tiles;
 
-  if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], SLOT_THREADS);
+  // The finish kernel may be scheduled on SMs as they free up; it waits for
+  // this whole grid (and its memory) before it reads anything this grid writes.
+  pdl_launch_dependents();
+
+  // Stage `n` (unit n / 4, stage n % 4) into ring slot n % nslot; called by
+  // the whole control warp, one lane issues.
+  auto fill = [&](int n) {
+    const int u = u_begin + n / NSTAGE, q = n % NSTAGE;
+    const int h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT + q * QT, s = n % nslot;
+    unsigned char *st = ring + s * sbytes;
+    if (tc::elect_one()) {
+      tc::mbar_arrive_expect_tx(&full[s], uint32_t(sbytes));
+      tc::tma_load_3d(st, &tm_part, h0, t0, 0, &full[s]);
+      tc::tma_load_3d(st + slot_res(p.tp), &tm_res, h0, 0, t0, &full[s]);
+      tc::tma_load_2d(st + slot_post(p.tp), &tm_post, 0, t0, &full[s]);
+      tc::tma_load_2d(st + slot_comb(p.tp), &tm_comb, 0, t0, &full[s]);
     }
-    tc::mbar_init(&mma_bar[0], 1);
-    tc::mbar_init(&mma_bar[1], 1);
-    *cabort_s = 0;
-    tc::mbar_init_fence();
+    __syncwarp();
+  };
+  // Whether the phase with `parity` of `bar` has completed, the same answer
+  // on every lane of the warp.
+  auto ready = [&](uint64_t *bar, uint32_t parity) {
+    return __shfl_sync(0xffffffffu, tc::mbar_test_wait(bar, parity) ? 1 : 0, 0) != 0;
+  };
+
+  if (warp == CTRL_WARP) {
+    if (tc::elect_one()) {
+      for (int s = 0; s < nslot; ++s) {
+        tc::mbar_init(&full[s], 1);
+        tc::mbar_init(&empty[s], STAGE_WARPS);
+      }
+      tc::mbar_init(afull, MIX_WARPS);
+      tc::mbar_init(&mma_bar[0], 1);
+      tc::mbar_init(&mma_bar[1], 1);
+      *abort_s = 0;
+      tc::mbar_init_fence();
+      tc::tma_prefetch_desc(&tm_part);
+      tc::tma_prefetch_desc(&tm_res);
+      tc::tma_prefetch_desc(&tm_post);
+      tc::tma_prefetch_desc(&tm_comb);
+    }
+    __syncwarp();
+    for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
+    // the later groups' hc_fn rows, so that their B builds read L2
+    const int last_group = (u_end - 1) / n_tiles;
+    for (int g = first_group + 1; g <= last_group && g <= first_group + 16; ++g) {
+      const int rows = p.hidden - g * UK < UK ? p.hidden - g * UK : UK;
+      for (int j = 0; j < HC; ++j) {
+        const float *src = p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX;
+        if (tc::elect_one()) tc::prefetch_l2(src, uint32_t(rows * MIX * 4));
+        __syncwarp();
+      }
+    }
+    tc::tmem_alloc(slot, TMEM_COLS);
+  } else {
+    build_b(p, first_group * UK, b_s);   // the first group's B, while the pipeline starts
   }
-  if (warp == 0) tc::tmem_alloc(slot, TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
 
-  const uint32_t idesc = tc::idesc_bf16_f32(ROWS, UN);
-  const int q = warp & 3, half = warp >> 2, f = lane & (FRAGS - 1);
-  // this thread's two tokens of stage q
-  int tl[2];
-  tl[0] = 4 * half + (lane >> 4);
-  tl[1] = tl[0] + 2;
-  unsigned char *stage = smem + Layout::stages + size_t(q) * STAGE_BYTES;
-  bool ok = true;
-  const bool filler = half == 0 && lane == 0;   // issues slot q's copies
-  const uint32_t tx = uint32_t(p.tp) * QT * ROW + QT * HC * ROW + QT * HC * 4 + QT * HC * HC * 4;
-  int fills = 0;                                 // copies issued into slot q (by the filler)
-  auto fill = [&](int n) {
-    const int u = u_begin + n, h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT + q * QT;
-    tc::mbar_arrive_expect_tx(&full[q], tx);
-    tc::tma_load_3d(stage + STAGE_PART, &tm_part, h0, t0, 0, &full[q]);
-    tc::tma_load_3d(stage + STAGE_RES, &tm_res, h0, 0, t0, &full[q]);
-    tc::tma_load_2d(stage + STAGE_POST, &tm_post, 0, t0, &full[q]);
-    tc::tma_load_2d(stage + STAGE_COMB, &tm_comb, 0, t0, &full[q]);
-    fills = n + 1;
-  };
-  if (filler && n_units > 0) {
-    tc::tma_prefetch_desc(&tm_part);
-    tc::tma_prefetch_desc(&tm_res);
-    tc::tma_prefetch_desc(&tm_post);
-    tc::tma_prefetch_desc(&tm_comb);
-    fill(0);
-  }
-
-  int cur_group = -1, pending = -1, issued = -1;
-  for (int i = 0; i < n_units; ++i) {
-    const int u = u_begin + i, gc = u / n_tiles, tile = u % n_tiles;
-    if (gc != cur_group) {
-      // B is about to change: the previous unit's MMAs must be done with it
-      if (pending >= 0) epilogue(p, tmem, mma_bar, pending, u_begin, n_tiles, q, half, ok);
-      pending = -1;
-      cta_sync();
-      build_b(p, gc * UK, b_s);
-      tc::fence_proxy_async_smem();
-      cta_sync();
-      cur_group = gc;
-    }
-    const int h = gc * UK + f * VEC;
-    if (ok && !tc::mbar_wait_bounded(&full[q], i & 1, WAIT_LIMIT)) ok = false;
-    Item it[2];
-    if (ok) {
-      load_item(p.tp, stage, tl[0], f, it[0]);
-      load_item(p.tp, stage, tl[1], f, it[1]);
-    }
-    // The slot's next fill is an async-proxy write: the generic-proxy reads
-    // above are ordered before it by a proxy fence ahead of the release.
-    tc::fence_proxy_async_smem();
-    tc::mbar_arrive(&empty[q]);
-    // once both warps of the slot hold unit i's stage, the slot takes unit i + 1's
-    if (filler && ok && i + 1 < n_units) {
-      if (tc::mbar_wait_bounded(&empty[q], i & 1, WAIT_LIMIT))
-        fill(i + 1);
-      else
-        ok = false;
-    }
-    uint4 yb[2], nv[2][HC];
-    float ss[2];
-    mix_pair(p.tp, it, yb, nv, ss);
+  if (warp == CTRL_WARP) {
+    // Event loop of the whole warp: refill released slots, issue the MMAs of
+    // complete A operands; it never blocks on one event while the other is ready.
+    int nf = nslot < total_fills ? nslot : total_fills, nm = 0;
+    uint32_t idle = 0;
+    const uint32_t idesc = tc::idesc_bf16_f32(ROWS, UN);
+    const uint64_t a0 = tc::smem_desc(tc::smem_addr(a_s), A_KCOL, 128);
+    const uint64_t b0 = tc::smem_desc(tc::smem_addr(b_s), B_KCOL, 128);
+    while (nf < total_fills || nm < n_units) {
+      bool progress = false;
+      if (nf < total_fills && ready(&empty[nf % nslot], uint32_t((nf / nslot - 1) & 1))) {
+        fill(nf++);
+        progress = true;
+      }
+      if (nm < n_units && ready(afull, uint32_t(nm & 1))) {
+        tc::fence_after_sync();
+        const uint32_t d = tmem + uint32_t(nm & 1) * D_STRIDE;
+        if (tc::elect_one()) {
+#pragma unroll 1
+          for (int term = 0; term < 3; ++term) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int t = tile * UT + q * QT + tl[k];
-      if (ok && t < p.m && h < p.hidden) {
-        if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb[k]);
-#pragma unroll
-        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[k][j]);
-      } else {
-        // columns past H and tokens past m contribute nothing to the GEMV
-#pragma unroll
-        for (int j = 0; j < HC; ++j) nv[k][j] = make_uint4(0, 0, 0, 0);
-        ss[k] = 0.f;
+            for (int ks = 0; ks < UK / 16; ++ks) {
+              const uint64_t ad = a0 + uint64_t((2 * ks * A_KCOL) >> 4);
+              const uint64_t bd = b0 + uint64_t(((term * KCOLS + 2 * ks) * B_KCOL) >> 4);
+              tc::mma_bf16(d, ad, bd, idesc, (term | ks) != 0);
+            }
+          }
+          tc::mma_commit(&mma_bar[nm & 1]);
+        }
+        __syncwarp();
+        ++nm;
+        progress = true;
+      }
+      if (progress) {
+        idle = 0;
+      } else if (*abort_s || ++idle > WAIT_LIMIT) {
+        if (lane == 0) *abort_s = 1;
+        break;
+      } else if (idle > 32) {
+        __nanosleep(32);
       }
     }
-    // the A buffer is free once the previous unit's MMAs are done
-    if (pending >= 0) epilogue(p, tmem, mma_bar, pending, u_begin, n_tiles, q, half, ok);
+    // copies still in flight land, and issued MMAs complete, before exit
+    for (int n = nf - nslot < 0 ? 0 : nf - nslot; n < nf; ++n)
+      tc::mbar_wait_bounded(&full[n % nslot], uint32_t((n / nslot) & 1), WAIT_LIMIT);
+    if (nm > 0) tc::mbar_wait_bounded(&mma_bar[(nm - 1) & 1], uint32_t(((nm - 1) >> 1) & 1), WAIT_LIMIT);
+    __syncwarp();
+  } else {
+    const int q = warp / STAGE_WARPS, item = (warp % STAGE_WARPS) * 32 + lane;
+    const int tl = item / FRAGS, f = item % FRAGS;
+    Epi ep = {tmem, mma_bar, abort_s, -1, 0, 0};
+    int cur_group = first_group;
+    for (int i = 0; i < n_units; ++i) {
+      if (*abort_s) break;
+      const int u = u_begin + i, g = u / n_tiles, tile = u % n_tiles;
+      if (g != cur_group) {
+        // B is about to change: the previous unit's MMAs must be done with it
+        if (ep.i >= 0) epilogue(p, ep);
+        ep.i = -1;
+        build_b(p, g * UK, b_s);
+        cur_group = g;
+      }
+      const int n = i * NSTAGE + q, s = n % nslot;
+      if (!tc::mbar_wait_bounded(&full[s], uint32_t((n / nslot) & 1), WAIT_LIMIT)) {
+        *abort_s = 1;
+        break;
+      }
+      Item it;
+      load_item(p.tp, ring + s * sbytes, tl, f, it);
+      // The slot's next fill is an async-proxy write: the generic-proxy reads
+      // above are ordered before it by a proxy fence ahead of the release.
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[s]);
+      uint4 yb, nv[HC];
+      float ss = mix_item(it, yb, nv);
+      const int t = tile * UT + q * QT + tl, h = g * UK + f * VEC;
+      if (t < p.m && h < p.hidden) {
+        if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
+      }
+      // the A buffer is free once the previous unit's MMAs are done
+      if (ep.i >= 0) epilogue(p, ep);
 #pragma unroll
       for (int j = 0; j < HC; ++j) {
-        const int row = 32 * q + 4 * tl[k] + j;
-        *reinterpret_cast<uint4 *>(a_s + size_t(f) * A_KCOL + (row / 8) * 128 + (row % 8) * 16) = nv[k][j];
+        const int row = 32 * q + 4 * tl + j;
+        *reinterpret_cast<uint4 *>(a_s + f * A_KCOL + (row >> 3) * 128 + (row & 7) * 16) = nv[j];
       }
       // the 16 fragments of a token are 16 consecutive lanes
-      float s = ss[k];
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      s += __shfl_xor_sync(0xffffffffu, s, 8);
-      const int t = tile * UT + q * QT + tl[k];
-      if (f == 0 && ok && t < p.m) p.part[(size_t)t * p.part_stride + gc * VALUES + MIX] = s;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+      if (f == 0 && t < p.m) p.part[(size_t)t * p.part_stride + g * VALUES + MIX] = ss;
+      // hand the A rows to the tensor core
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(afull);
+      ep.i = i;
+      ep.tile = tile;
+      ep.group = g;
     }
-    pending = -1;
-    // hand the A buffer to the tensor core
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    if (!ok) *cabort_s = 1;
-    cta_sync();
-    if (*cabort_s) {
-      ok = false;
-      break;
-    }
-    if (tid == 0) {
-      tc::fence_after_sync();
-      const uint32_t a_addr = tc::smem_addr(a_s), b_addr = tc::smem_addr(b_s);
-      const uint32_t d = uint32_t(i & 1) * D_STRIDE;
-#pragma unroll 1
-      for (int term = 0; term < 3; ++term) {
-#pragma unroll
-        for (int ks = 0; ks < UK / 16; ++ks) {
-          const uint64_t ad = tc::smem_desc(a_addr + uint32_t(2 * ks * A_KCOL), A_KCOL, 128);
-          const uint64_t bd = tc::smem_desc(b_addr + uint32_t((term * KCOLS + 2 * ks) * B_KCOL), B_KCOL, 128);
-          tc::mma_bf16(tmem + d, ad, bd, idesc, (term | ks) != 0);
-        }
-      }
-      tc::mma_commit(&mma_bar[i & 1]);
-    }
-    pending = issued = i;
-  }
-  if (pending >= 0) epilogue(p, tmem, mma_bar, pending, u_begin, n_tiles, q, half, ok);
-  // copies still in flight land before the CTA may exit
-  if (filler && fills > 0) tc::mbar_wait_bounded(&full[q], (fills - 1) & 1, WAIT_LIMIT);
-  if (!ok && tid == 0) {
-    if (p.err) atomicOr(p.err, 2u);
-    // MMAs still in flight finish before their tensor memory is released
-    if (issued >= 0) tc::mbar_wait_bounded(&mma_bar[issued & 1], (issued >> 1) & 1, WAIT_LIMIT);
+    if (ep.i >= 0 && !*abort_s) epilogue(p, ep);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == CTRL_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
+  if (tid == 0 && *abort_s && p.err) atomicOr(p.err, 2u);
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -478,11 +530,11 @@ bool encode(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *ba
 
 }  // namespace
 
-size_t stage_tc_smem_bytes() { return Layout::total; }
+size_t stage_tc_smem_bytes() { return size_t(SMEM_MAX); }
 
 cudaError_t stage_tc_set_attributes() {
   if (!encode_fn()) return cudaErrorNotSupported;
-  return cudaFuncSetAttribute(k_stage_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Layout::total));
+  return cudaFuncSetAttribute(k_stage_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
 }
 
 cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream) {
@@ -505,7 +557,8 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
     return cudaErrorInvalidValue;
   const int units = ((p.m + UT - 1) / UT) * p.slices;
   const int grid = units < ctas ? units : ctas;
-  k_stage_tc<<<grid, NT, Layout::total, stream>>>(p, tm_part, tm_res, tm_post, tm_comb);
+  const size_t smem = size_t(Layout::ring) + size_t(ring_slots(p.tp)) * slot_bytes(p.tp);
+  k_stage_tc<<<grid, NT, smem, stream>>>(p, tm_part, tm_res, tm_post, tm_comb);
   return cudaGetLastError();
 }
 

@@ -49,8 +49,9 @@ struct StageParams {
                               // bit 1: a tensor-core completion wait gave up)
 };
 
-// Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm
-// and the optional MXFP8 copy.
+// Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm,
+// the optional MXFP8 copy and, with post_out / comb_out set, the next
+// boundary's post-mix and Sinkhorn mix.
 struct FinishParams {
   int m, hidden, slices, part_stride;
   const float *part;
@@ -59,13 +60,28 @@ struct FinishParams {
   const uint16_t *gamma;
   const uint16_t *streams;    // the residual_out the stage kernel wrote
   float rms_eps, hc_eps, norm_eps;
-  float *mixes;               // [m][24] raw mixes for the side kernel
+  float *mixes;               // [m][24] raw mixes for the side kernel, or null
   float *mixes_out;           // optional copy
+  float *post_out;            // [m][4]: post-mix computed here (fused), or null
+  float *comb_out;            // [m][4][4]: Sinkhorn mix computed here (fused), or null
+  float post_mult;
+  int repeat;                 // Sinkhorn rounds
   float *pre_out;             // optional
   uint16_t *layer_input;      // [m][H]
   uint8_t *mx_values;         // [m][H] or null
   uint8_t *mx_scales;         // mxfp8_scale_bytes(m, H) or null
   unsigned int *err;          // device error word (bit 1: a wait gave up) or null
+};
+
+// MoE fold: stage 1 of a MoE-finalize call into a [m][H] BF16 buffer.
+struct FoldParams {
+  int m, hidden, tp, top_k, rows_per_rank;
+  const uint16_t *routed;     // [tp][rows][H]
+  const int32_t *idx;         // [tp][m][K]
+  const float *weights;       // [m][K]
+  const uint16_t *shared;     // [tp][m][H]
+  uint16_t *y;                // [m][H]
+  unsigned int *err;          // bit 0: route index outside [-1, rows)
 };
 
 // Side kernel: post-mix and Sinkhorn residual mix of the next boundary.
@@ -94,5 +110,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
 cudaError_t finish_set_attributes();
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
+// MoE fold over at most `ctas` CTAs of 128 threads.
+cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream);
 
 }  // namespace mhc

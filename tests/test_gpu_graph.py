@@ -1,6 +1,7 @@
 """Boundary calls recorded into a CUDA graph give the same bits as eager
-calls, including the side-stream outputs (post, comb) that the capture joins
-back before it ends, and the graph can be replayed."""
+calls, including post and comb (computed in the finish kernel, or by the
+side-stream kernel that the capture joins back before it ends), and the graph
+can be replayed."""
 import numpy as np
 import pytest
 import torch
@@ -15,12 +16,13 @@ def _bytes(outs):
     return {k: v.view(torch.uint8).cpu().numpy() for k, v in outs.items()}
 
 
-def test_captured_calls_match_eager_calls():
+@pytest.mark.parametrize("side_mixes", [False, True])
+def test_captured_calls_match_eager_calls(side_mixes):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     from mhc_residual_boundary_gb300 import Boundary
     hidden, tp, m = 2048, 4, 40
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, mxfp8=True)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, mxfp8=True, side_mixes=side_mixes)
     try:
         ins = [to_device(synth.make_inputs(hidden, tp, m, seed=s)) for s in (31, 32)]
         eager = []

@@ -96,23 +96,30 @@ def test_other_scalars(Boundary):
           norm_eps=1e-2, seed=9)
 
 
-def test_sync_mixes_flag_gives_same_bits(Boundary):
+MIXES_PLACEMENTS = {"fused": {}, "side": {"side_mixes": True}, "sync": {"sync_mixes": True}}
+
+
+def test_mixes_placements_give_same_bits(Boundary):
+    # post / Sinkhorn inside the finish kernel, in the side-stream kernel and
+    # in the same kernel on the caller's stream take the same operations
     inp = synth.make_inputs(1024, 4, 50, seed=3)
-    outs = []
-    for sync in (False, True):
-        b = Boundary(hidden=1024, tp=4, max_num_tokens=50, sync_mixes=sync)
-        outs.append(run_gpu(b, inp))
+    outs = {}
+    for name, flags in MIXES_PLACEMENTS.items():
+        b = Boundary(hidden=1024, tp=4, max_num_tokens=50, **flags)
+        outs[name] = run_gpu(b, inp)
         b.close()
-    for name in outs[0]:
-        assert np.array_equal(outs[0][name], outs[1][name]), name
+    for name in outs["fused"]:
+        for other in ("side", "sync"):
+            assert np.array_equal(outs["fused"][name], outs[other][name]), (name, other)
 
 
-def test_back_to_back_calls_chain_mixes(Boundary):
-    # call 2 reads call 1's post_out / comb_out on the same stream: the
-    # automatic join must order it after the side kernel
+@pytest.mark.parametrize("placement", sorted(MIXES_PLACEMENTS))
+def test_back_to_back_calls_chain_mixes(Boundary, placement):
+    # call 2 reads call 1's post_out / comb_out on the same stream: with the
+    # side-stream kernel the automatic join must order it after that kernel
     hidden, tp, m = 2048, 4, 64
     inp = synth.make_inputs(hidden, tp, m, seed=5)
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, **MIXES_PLACEMENTS[placement])
     dev = to_device(inp)
     o1 = b.empty_outputs(m, extras=True)
     b.run(dev, o1)
