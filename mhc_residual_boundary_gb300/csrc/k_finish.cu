@@ -109,13 +109,23 @@ __device__ __forceinline__ float sum4(float a, float b, float c, float d) {
   return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
 }
 
-__device__ __noinline__ void post_and_sinkhorn(const FinishParams &p, int t, const float *mix) {
+// Its arguments are values, not the kernel's parameter block by reference
+// (an out-of-line function would read that through a generic pointer into
+// parameter space, which is slow).
+struct MixArgs {
+  const float *scale, *base;
+  float *post_out, *comb_out;
+  float post_mult, eps;
+  int repeat;
+};
+
+__device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const float *mix) {
 #pragma unroll
   for (int j = 0; j < HC; ++j) {
     const float z = __fadd_rn(__fmul_rn(mix[HC + j], p.scale[1]), p.base[HC + j]);
     p.post_out[(size_t)t * HC + j] = __fmul_rn(sigmoid(z), p.post_mult);
   }
-  const float eps = p.hc_eps, s2 = p.scale[2];
+  const float eps = p.eps, s2 = p.scale[2];
   float c[HC * HC];
 #pragma unroll
   for (int i = 0; i < HC * HC; ++i) c[i] = __fadd_rn(__fmul_rn(mix[2 * HC + i], s2), p.base[2 * HC + i]);
@@ -222,7 +232,8 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
       }
       __syncwarp();
       if (p.post_out && (b == BATCH - 1 || k == n_tok - 1)) {
-        if (lane <= b) post_and_sinkhorn(p, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
+        const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
+        if (lane <= b) post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
         __syncwarp();
       }
     } else {
@@ -235,7 +246,7 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
       }
       uint16_t *sv = reinterpret_cast<uint16_t *>(slot);
       float ssq = 0.f;
-#pragma unroll 1
+#pragma unroll 2
       for (int fr = tid; fr < nfrag; fr += CT) {
         float n0[8], n1[8], n2[8], n3[8], c[8];
         uint16_t *s = sv + (size_t)fr * VEC;
@@ -260,7 +271,7 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
       const float ir = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(sq, float(H)), p.norm_eps)));
 
       // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
-#pragma unroll 1
+#pragma unroll 2
       for (int base = 0; base < nfrag; base += CT) {
         const int fr = base + tid;
         const bool live = fr < nfrag;

@@ -4,15 +4,16 @@
 // Work unit: 32 tokens x one group of 128 hidden columns (every row piece a
 // unit reads is a 256-byte run).  Units are numbered group-major and every
 // CTA (one per SM, persistent) takes a contiguous range of them, so a CTA
-// stages each group's hc_fn once.  Roles in a CTA of 17 warps:
+// stages each group's hc_fn once.  Roles in a CTA of 18 warps:
 //
-//   control warp: an event loop that never blocks (one lane issues).  It refills ring
-//     slots as soon as the mixer warps release them -- stage q (tokens
-//     8q .. 8q+7) of every unit by four TMA tensor copies: the partials
-//     [tp][m][H] (one 3-D box of 128 columns x 8 tokens x tp ranks), the
-//     residual streams [m][4][H], post [m][4] and comb [m][4][4], counted on
-//     the slot's mbarrier; out-of-range tokens and columns arrive as zeros --
-//     and it issues a unit's MMAs as soon as its A operand is complete.
+//   producer warp (one lane issues): refills ring slots as soon as the mixer
+//     warps release them -- stage q (tokens 8q .. 8q+7) of every unit by four
+//     TMA tensor copies: the partials [tp][m][H] (one 3-D box of 128 columns
+//     x 8 tokens x tp ranks), the residual streams [m][4][H], post [m][4] and
+//     comb [m][4][4], counted on the slot's mbarrier; out-of-range tokens and
+//     columns arrive as zeros.
+//   MMA warp (one lane issues): a unit's MMAs as soon as its A operand is
+//     complete; it also owns the tensor memory.
 //   16 mixer warps: four per stage, one (token, 16-byte fragment) item per
 //     thread.  Stage-1 sum of the tp partials in FP32 in rank order, rounded
 //     to BF16 ([DSV] _LamportMHCDeviceKernel.kernel, lane_sum); post-mix of
@@ -37,9 +38,10 @@
 //     sums go to the scratch rows [m][groups][25] (24 sums + the sum of
 //     squares; rows padded to 16 bytes) that the finish kernel reduces.
 //
-// The mixers build the first group's B while the control warp starts the
-// pipeline, and the later groups' hc_fn rows are prefetched into L2, so a
-// later B build does not wait on DRAM.  Every wait is bounded; a wait that gives up sets bit 1 of the error
+// A group's hc_fn rows (FP32) arrive by four bulk copies into the A buffer,
+// which is idle at that point, and the mixers split them into B from shared
+// memory; the producer issues the first group's copies before anything else
+// and prefetches the later groups' rows into L2.  Every wait is bounded; a wait that gives up sets bit 1 of the error
 // word and stops the CTA.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
@@ -57,8 +59,9 @@ namespace mhc {
 namespace {
 
 constexpr int MIX_WARPS = 16;                 // mixer warps
-constexpr int CTRL_WARP = MIX_WARPS;          // the control warp's index
-constexpr int NT = (MIX_WARPS + 1) * 32;      // 544 threads
+constexpr int PROD_WARP = MIX_WARPS;          // the TMA producer warp
+constexpr int MMA_WARP = MIX_WARPS + 1;       // the MMA warp
+constexpr int NT = (MIX_WARPS + 2) * 32;      // 576 threads
 constexpr int MIX_THREADS = MIX_WARPS * 32;
 constexpr int UT = 32;                        // tokens per unit
 constexpr int ROWS = HC * UT;                 // MMA M: (token, stream) rows
@@ -81,24 +84,28 @@ constexpr uint32_t WAIT_LIMIT = 1u << 22;     // polls before a wait gives up
 constexpr int SMEM_MAX = 227 * 1024;          // dynamic shared memory of one CTA
 constexpr int B_PAIRS = (UK / 2) * UN / MIX_THREADS;   // hc_fn element pairs per mixer thread
 constexpr int OUTS = MIX / STAGE_WARPS;       // outputs one epilogue warp reads per block (6)
+constexpr int HC_ROWS_BYTES = UK * MIX * 4;   // one stream's hc_fn rows of a group (FP32)
+constexpr int STAGING = HC * HC_ROWS_BYTES;   // a group's hc_fn rows, staged over the A buffer
 static_assert(QT * FRAGS == STAGE_WARPS * 32, "one item per mixer thread");
 static_assert(ROWS == 4 * 32 && QT * HC == 32, "one TMEM lane quarter per stage");
 static_assert((UK / 2) * UN % MIX_THREADS == 0 && B_PAIRS == 12, "B build split");
 static_assert(OUTS == 6, "epilogue split: four outputs plus two");
 static_assert(UK % 16 == 0 && UN % 16 == 0 && UN <= 256, "MMA shape");
 
-// Shared memory: control block, A, B, then the ring of stage slots.
+// Shared memory: control block, B, A (whose space also takes a group's
+// staged hc_fn rows), then the ring of stage slots.
 struct Layout {
   static constexpr int full = 0;                        // uint64 [MAX_SLOTS]
   static constexpr int empty = full + 8 * MAX_SLOTS;    // uint64 [MAX_SLOTS]
   static constexpr int afull = empty + 8 * MAX_SLOTS;   // uint64: A operand complete
   static constexpr int mma = afull + 8;                 // uint64 [2]: MMAs of a unit done
-  static constexpr int slot = mma + 16;                 // TMEM address
+  static constexpr int bfull = mma + 16;                // uint64: a group's hc_fn rows staged
+  static constexpr int slot = bfull + 8;                // TMEM address
   static constexpr int abort = slot + 4;                // int
-  static constexpr int a = 256;
-  static constexpr int b = a + A_BYTES;
-  static constexpr int ring = b + B_BYTES;
-  static_assert(abort + 4 <= a, "control block");
+  static constexpr int b = 256;
+  static constexpr int a = b + B_BYTES;
+  static constexpr int ring = a + (A_BYTES > STAGING ? A_BYTES : STAGING);
+  static_assert(abort + 4 <= b, "control block");
   static_assert(a % 128 == 0 && b % 128 == 0 && ring % 128 == 0, "TMA / MMA alignment");
 };
 
@@ -153,27 +160,20 @@ __device__ __forceinline__ void b_pair(int e, int &kp, int &n) {
   n = (rest % 12) * 8 + ((e >> 2) & 7);
 }
 
-__device__ __forceinline__ void load_b(const StageParams &p, int h0, float (&x0)[B_PAIRS], float (&x1)[B_PAIRS]) {
-  const int tid = threadIdx.x;
-#pragma unroll
+// Splits the group's staged hc_fn rows (stream j's rows at stg + j * 128 * 24
+// floats; rows past `rows` are treated as zero) into B.  A plain loop: the
+// code is short, and every load is a shared-memory read.
+__device__ __noinline__ void convert_b(const float *stg, int rows, unsigned char *b_s) {
+#pragma unroll 2
   for (int it = 0; it < B_PAIRS; ++it) {
     int kp, n;
-    b_pair(tid + it * MIX_THREADS, kp, n);
-    const int j = n / MIX, i = n % MIX, h = h0 + 2 * kp;
-    const float *src = p.hc_fn + ((size_t)j * p.hidden + h) * MIX + i;
-    x0[it] = h < p.hidden ? __ldg(src) : 0.f;
-    x1[it] = h + 1 < p.hidden ? __ldg(src + MIX) : 0.f;
-  }
-}
-
-__device__ __forceinline__ void store_b(unsigned char *b_s, const float (&x0)[B_PAIRS], const float (&x1)[B_PAIRS]) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int it = 0; it < B_PAIRS; ++it) {
-    int kp, n;
-    b_pair(tid + it * MIX_THREADS, kp, n);
-    const uint32_t hi = pack_bf16x2(x0[it], x1[it]);
-    const float r0 = __fsub_rn(x0[it], bf16_lo(hi)), r1 = __fsub_rn(x1[it], bf16_hi(hi));
+    b_pair(threadIdx.x + it * MIX_THREADS, kp, n);
+    const int j = n / MIX, i = n % MIX, k = 2 * kp;
+    const float *src = stg + (j * UK + k) * MIX + i;
+    const float x0 = k < rows ? src[0] : 0.f;
+    const float x1 = k + 1 < rows ? src[MIX] : 0.f;
+    const uint32_t hi = pack_bf16x2(x0, x1);
+    const float r0 = __fsub_rn(x0, bf16_lo(hi)), r1 = __fsub_rn(x1, bf16_hi(hi));
     const uint32_t mid = pack_bf16x2(r0, r1);
     const uint32_t lo = pack_bf16x2(__fsub_rn(r0, bf16_lo(mid)), __fsub_rn(r1, bf16_hi(mid)));
     unsigned char *dst = b_s + (kp >> 2) * B_KCOL + (n >> 3) * 128 + (n & 7) * 16 + (kp & 3) * 4;
@@ -183,12 +183,19 @@ __device__ __forceinline__ void store_b(unsigned char *b_s, const float (&x0)[B_
   }
 }
 
-// Loads the group's hc_fn and stores its three BF16 terms (all loads are
-// issued before the first split, so the build costs one memory latency).
-__device__ __noinline__ void build_b(const StageParams &p, int h0, unsigned char *b_s) {
-  float x0[B_PAIRS], x1[B_PAIRS];
-  load_b(p, h0, x0, x1);
-  store_b(b_s, x0, x1);
+// Rows of group g (at most 128; fewer in the last group).
+__device__ __forceinline__ int group_rows(int hidden, int g) {
+  return hidden - g * UK < UK ? hidden - g * UK : UK;
+}
+
+// One lane: the four bulk copies of group g's hc_fn rows into `stg`, counted
+// on `bar`.
+__device__ __forceinline__ void stage_hc_fn(const StageParams &p, int g, unsigned char *stg, uint64_t *bar) {
+  const int rows = group_rows(p.hidden, g);
+  tc::mbar_arrive_expect_tx(bar, uint32_t(HC * rows * MIX * 4));
+  for (int j = 0; j < HC; ++j)
+    tc::bulk_load(stg + j * HC_ROWS_BYTES, p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX,
+                  uint32_t(rows * MIX * 4), bar);
 }
 
 // ------------------------------------------------------------- epilogue
@@ -197,14 +204,19 @@ __device__ __noinline__ void build_b(const StageParams &p, int h0, unsigned char
 // 4s .. 4s+3 and 16+2s, 17+2s (s = w / 4) of all four stream blocks; each
 // lane takes its own stream's block, the four lanes of a token add them in
 // the order ((j0 + j1) + (j2 + j3)) and lane o % 4 writes output o.
+// Everything it reads is passed by value: an out-of-line function that took
+// the kernel's parameter block by reference would read every field through a
+// generic pointer into parameter space, which is slow.
 struct Epi {
+  float *part;             // the partial-sum scratch
+  int part_stride, m;
   uint32_t tmem;
   uint64_t *mma_bar;
   volatile int *abort_s;
   int i, tile, group;
 };
 
-__device__ __noinline__ void epilogue(const StageParams &p, const Epi &e) {
+__device__ __noinline__ void epilogue(const Epi e) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3, s = warp >> 2, j = lane & 3, d = e.i & 1;
   const bool ok = tc::mbar_wait_bounded(&e.mma_bar[d], (e.i >> 1) & 1, WAIT_LIMIT);
@@ -224,7 +236,7 @@ __device__ __noinline__ void epilogue(const StageParams &p, const Epi &e) {
     tc::tmem_hold2(r2[jb]);
   }
   const int t = e.tile * UT + q * QT + (lane >> 2);
-  float *dst = p.part + (size_t)t * p.part_stride + e.group * VALUES;
+  float *dst = e.part + (size_t)t * e.part_stride + e.group * VALUES;
 #pragma unroll
   for (int o = 0; o < OUTS; ++o) {
     const int c = o < 4 ? o : o - 4;
@@ -234,7 +246,7 @@ __device__ __noinline__ void epilogue(const StageParams &p, const Epi &e) {
     float sum = v + __shfl_xor_sync(0xffffffffu, v, 1);
     sum = sum + __shfl_xor_sync(0xffffffffu, sum, 2);
     const int out = o < 4 ? 4 * s + o : 16 + 2 * s + (o - 4);
-    if (ok && j == (o & 3) && t < p.m) dst[out] = sum;
+    if (ok && j == (o & 3) && t < e.m) dst[out] = sum;
   }
 }
 
@@ -301,7 +313,7 @@ __device__ __forceinline__ float mix_item(Item &it, uint4 &yb, uint4 (&nv)[HC]) 
 }
 
 // ------------------------------------------------------------------ kernel
-// 17 warps put five on one SM sub-partition (16384 registers each), so a
+// 18 warps put five on one SM sub-partition (16384 registers each), so a
 // thread may use at most 96 registers.
 __global__ void __launch_bounds__(NT, 1)
     k_stage_tc(const StageParams p, const __grid_constant__ CUtensorMap tm_part,
@@ -312,6 +324,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Layout::empty);
   uint64_t *afull = reinterpret_cast<uint64_t *>(smem + Layout::afull);
   uint64_t *mma_bar = reinterpret_cast<uint64_t *>(smem + Layout::mma);
+  uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + Layout::bfull);
   uint32_t *slot = reinterpret_cast<uint32_t *>(smem + Layout::slot);
   volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Layout::abort);
   unsigned char *a_s = smem + Layout::a;
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(NT, 1)
   pdl_launch_dependents();
 
   // Stage `n` (unit n / 4, stage n % 4) into ring slot n % nslot; called by
-  // the whole control warp, one lane issues.
+  // the whole producer warp, one lane issues.
   auto fill = [&](int n) {
     const int u = u_begin + n / NSTAGE, q = n % NSTAGE;
     const int h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT + q * QT, s = n % nslot;
@@ -347,13 +360,8 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncwarp();
   };
-  // Whether the phase with `parity` of `bar` has completed, the same answer
-  // on every lane of the warp.
-  auto ready = [&](uint64_t *bar, uint32_t parity) {
-    return __shfl_sync(0xffffffffu, tc::mbar_test_wait(bar, parity) ? 1 : 0, 0) != 0;
-  };
 
-  if (warp == CTRL_WARP) {
+  if (warp == PROD_WARP) {
     if (tc::elect_one()) {
       for (int s = 0; s < nslot; ++s) {
         tc::mbar_init(&full[s], 1);
@@ -362,8 +370,11 @@ __global__ void __launch_bounds__(NT, 1)
       tc::mbar_init(afull, MIX_WARPS);
       tc::mbar_init(&mma_bar[0], 1);
       tc::mbar_init(&mma_bar[1], 1);
+      tc::mbar_init(bfull, 1);
       *abort_s = 0;
       tc::mbar_init_fence();
+      // the first group's hc_fn rows before anything else
+      stage_hc_fn(p, first_group, a_s, bfull);
       tc::tma_prefetch_desc(&tm_part);
       tc::tma_prefetch_desc(&tm_res);
       tc::tma_prefetch_desc(&tm_post);
@@ -371,85 +382,93 @@ __global__ void __launch_bounds__(NT, 1)
     }
     __syncwarp();
     for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
-    // the later groups' hc_fn rows, so that their B builds read L2
+    // the later groups' hc_fn rows, so that their staging copies read L2
     const int last_group = (u_end - 1) / n_tiles;
     for (int g = first_group + 1; g <= last_group && g <= first_group + 16; ++g) {
-      const int rows = p.hidden - g * UK < UK ? p.hidden - g * UK : UK;
+      const uint32_t bytes = uint32_t(group_rows(p.hidden, g) * MIX * 4);
       for (int j = 0; j < HC; ++j) {
         const float *src = p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX;
-        if (tc::elect_one()) tc::prefetch_l2(src, uint32_t(rows * MIX * 4));
+        if (tc::elect_one()) tc::prefetch_l2(src, bytes);
         __syncwarp();
       }
     }
+  } else if (warp == MMA_WARP) {
     tc::tmem_alloc(slot, TMEM_COLS);
-  } else {
-    build_b(p, first_group * UK, b_s);   // the first group's B, while the pipeline starts
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
 
-  if (warp == CTRL_WARP) {
-    // Event loop of the whole warp: refill released slots, issue the MMAs of
-    // complete A operands; it never blocks on one event while the other is ready.
-    int nf = nslot < total_fills ? nslot : total_fills, nm = 0;
-    uint32_t idle = 0;
+  if (warp == PROD_WARP) {
+    // refill each slot as soon as its previous stage has been read
+    int nf = nslot < total_fills ? nslot : total_fills;
+    for (; nf < total_fills; ++nf) {
+      const int s = nf % nslot;
+      if (!tc::mbar_wait_bounded(&empty[s], uint32_t((nf / nslot - 1) & 1), WAIT_LIMIT) || *abort_s) {
+        if (lane == 0) *abort_s = 1;
+        break;
+      }
+      fill(nf);
+    }
+    // copies still in flight land before exit
+    for (int n = nf - nslot < 0 ? 0 : nf - nslot; n < nf; ++n)
+      tc::mbar_wait_bounded(&full[n % nslot], uint32_t((n / nslot) & 1), WAIT_LIMIT);
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // a unit's 3 x 8 MMAs once its A operand is complete
     const uint32_t idesc = tc::idesc_bf16_f32(ROWS, UN);
     const uint64_t a0 = tc::smem_desc(tc::smem_addr(a_s), A_KCOL, 128);
     const uint64_t b0 = tc::smem_desc(tc::smem_addr(b_s), B_KCOL, 128);
-    while (nf < total_fills || nm < n_units) {
-      bool progress = false;
-      if (nf < total_fills && ready(&empty[nf % nslot], uint32_t((nf / nslot - 1) & 1))) {
-        fill(nf++);
-        progress = true;
-      }
-      if (nm < n_units && ready(afull, uint32_t(nm & 1))) {
-        tc::fence_after_sync();
-        const uint32_t d = tmem + uint32_t(nm & 1) * D_STRIDE;
-        if (tc::elect_one()) {
-#pragma unroll 1
-          for (int term = 0; term < 3; ++term) {
-#pragma unroll
-            for (int ks = 0; ks < UK / 16; ++ks) {
-              const uint64_t ad = a0 + uint64_t((2 * ks * A_KCOL) >> 4);
-              const uint64_t bd = b0 + uint64_t(((term * KCOLS + 2 * ks) * B_KCOL) >> 4);
-              tc::mma_bf16(d, ad, bd, idesc, (term | ks) != 0);
-            }
-          }
-          tc::mma_commit(&mma_bar[nm & 1]);
-        }
-        __syncwarp();
-        ++nm;
-        progress = true;
-      }
-      if (progress) {
-        idle = 0;
-      } else if (*abort_s || ++idle > WAIT_LIMIT) {
+    int nm = 0;
+    for (; nm < n_units; ++nm) {
+      if (!tc::mbar_wait_bounded(afull, uint32_t(nm & 1), WAIT_LIMIT) || *abort_s) {
         if (lane == 0) *abort_s = 1;
         break;
-      } else if (idle > 32) {
-        __nanosleep(32);
       }
+      tc::fence_after_sync();
+      const uint32_t d = tmem + uint32_t(nm & 1) * D_STRIDE;
+      if (tc::elect_one()) {
+#pragma unroll 1
+        for (int term = 0; term < 3; ++term) {
+#pragma unroll
+          for (int ks = 0; ks < UK / 16; ++ks) {
+            const uint64_t ad = a0 + uint64_t((2 * ks * A_KCOL) >> 4);
+            const uint64_t bd = b0 + uint64_t(((term * KCOLS + 2 * ks) * B_KCOL) >> 4);
+            tc::mma_bf16(d, ad, bd, idesc, (term | ks) != 0);
+          }
+        }
+        tc::mma_commit(&mma_bar[nm & 1]);
+      }
+      __syncwarp();
     }
-    // copies still in flight land, and issued MMAs complete, before exit
-    for (int n = nf - nslot < 0 ? 0 : nf - nslot; n < nf; ++n)
-      tc::mbar_wait_bounded(&full[n % nslot], uint32_t((n / nslot) & 1), WAIT_LIMIT);
+    // issued MMAs complete before the tensor memory is released
     if (nm > 0) tc::mbar_wait_bounded(&mma_bar[(nm - 1) & 1], uint32_t(((nm - 1) >> 1) & 1), WAIT_LIMIT);
     __syncwarp();
   } else {
     const int q = warp / STAGE_WARPS, item = (warp % STAGE_WARPS) * 32 + lane;
     const int tl = item / FRAGS, f = item % FRAGS;
-    Epi ep = {tmem, mma_bar, abort_s, -1, 0, 0};
-    int cur_group = first_group;
+    Epi ep = {p.part, p.part_stride, p.m, tmem, mma_bar, abort_s, -1, 0, 0};
+    int cur_group = -1, loads = 0;   // hc_fn groups staged so far
     for (int i = 0; i < n_units; ++i) {
       if (*abort_s) break;
       const int u = u_begin + i, g = u / n_tiles, tile = u % n_tiles;
       if (g != cur_group) {
-        // B is about to change: the previous unit's MMAs must be done with it
-        if (ep.i >= 0) epilogue(p, ep);
+        // B and the A space change: the previous unit's MMAs must be done
+        if (ep.i >= 0) epilogue(ep);
         ep.i = -1;
-        build_b(p, g * UK, b_s);
+        if (cur_group >= 0 && warp == 0) {
+          if (tc::elect_one()) stage_hc_fn(p, g, a_s, bfull);
+          __syncwarp();
+        }
+        if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
+          *abort_s = 1;
+          break;
+        }
+        ++loads;
+        convert_b(reinterpret_cast<const float *>(a_s), group_rows(p.hidden, g), b_s);
+        // every mixer has read the staged rows before any A row is written
+        asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
         cur_group = g;
       }
       const int n = i * NSTAGE + q, s = n % nslot;
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
       }
       // the A buffer is free once the previous unit's MMAs are done
-      if (ep.i >= 0) epilogue(p, ep);
+      if (ep.i >= 0) epilogue(ep);
 #pragma unroll
       for (int j = 0; j < HC; ++j) {
         const int row = 32 * q + 4 * tl + j;
@@ -485,7 +504,7 @@ __global__ void __launch_bounds__(NT, 1)
       ss += __shfl_xor_sync(0xffffffffu, ss, 4);
       ss += __shfl_xor_sync(0xffffffffu, ss, 8);
       if (f == 0 && t < p.m) p.part[(size_t)t * p.part_stride + g * VALUES + MIX] = ss;
-      // hand the A rows to the tensor core
+      // hand the A rows (and a new B) to the tensor core
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
@@ -494,12 +513,12 @@ __global__ void __launch_bounds__(NT, 1)
       ep.tile = tile;
       ep.group = g;
     }
-    if (ep.i >= 0 && !*abort_s) epilogue(p, ep);
+    if (ep.i >= 0 && !*abort_s) epilogue(ep);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == CTRL_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
   if (tid == 0 && *abort_s && p.err) atomicOr(p.err, 2u);
 }
 
