@@ -1,7 +1,8 @@
 // k_finish.cu -- finish kernel of the mHC boundary.  Per token:
 //
 //  1. sums the stage kernel's per-group partials in group order (24 GEMV
-//     outputs and the sum of squares of the new streams);
+//     outputs and the sum of squares of the new streams), one value per
+//     lane of the mixes warp;
 //  2. rstd = 1/sqrt(ss / (4H) + rms_eps), mixes = raw * rstd,
 //     pre_j = sigmoid(mixes_j * scale[0] + base[j]) + hc_eps
 //     ([GLM] _BoundaryDeviceKernel.kernel, "rstd", "pre_mix");
@@ -165,7 +166,7 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
 __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[MAX_SLOTS];
-  __shared__ float tot_s[VALUES];
+  __shared__ float pre_s[HC];
   __shared__ float red_s[CWARPS];
   __shared__ float mix_s[BATCH][MIX];
   __shared__ int abort_s;
@@ -187,12 +188,13 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
   // Nothing below may read the stage kernel's outputs before this point.
   pdl_wait();
 
+  const uint64_t read_once = tc::policy_evict_first();   // the new streams are read once more, here
   auto fill = [&](int k) {   // thread 0: token k of this CTA into slot k % slots
     const int t = int(blockIdx.x) + k * int(gridDim.x);
     unsigned char *dst = smem + size_t(k % slots) * sbytes;
     uint64_t *bar = &full[k % slots];
     tc::mbar_arrive_expect_tx(bar, stream_bytes + part_bytes);
-    tc::bulk_load(dst, p.streams + (size_t)t * HC * H, stream_bytes, bar);
+    tc::bulk_load_hint(dst, p.streams + (size_t)t * HC * H, stream_bytes, bar, read_once);
     tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, bar);
   };
   int filled = 0;   // tokens whose copies were issued (thread 0)
@@ -206,31 +208,33 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
     if (!tc::mbar_wait_bounded(&full[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) abort_s = 1;
     const float *part_s = reinterpret_cast<const float *>(slot + stream_bytes);
 
-    // 1. partial sums over the groups, in group order within each lane
-    for (int v = warp; v < VALUES; v += NT / 32) {
-      float s = 0.f;
-      for (int g = lane; g < p.slices; g += 32) s += part_s[g * VALUES + v];
-      s = warp_sum(s);
-      if (lane == 0) tot_s[v] = s;
+    // 1.-2. (mixes warp) each of lanes 0-24 sums one value over the groups
+    // in group order; rstd, the mixes, pre (shared with the collapse warps)
+    if (warp == MIX_WARP) {
+      float v = 0.f;
+      if (lane < VALUES)
+        for (int g = 0; g < p.slices; ++g) v = __fadd_rn(v, part_s[g * VALUES + lane]);
+      const float ss = __shfl_sync(0xffffffffu, v, MIX);
+      const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
+      if (lane < MIX) {
+        const float mix = __fmul_rn(v, rstd);
+        mix_s[k % BATCH][lane] = mix;
+        if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
+        if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
+        if (lane < HC) {
+          const float pre = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+          pre_s[lane] = pre;
+          if (p.pre_out) p.pre_out[(size_t)t * HC + lane] = pre;
+        }
+      }
     }
     __syncthreads();
     if (abort_s) break;
-    const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(tot_s[MIX], float(HC * H)), p.rms_eps)));
 
     if (warp == MIX_WARP) {
-      // 2. mixes and pre of this token; (fused) post + Sinkhorn per batch of
-      // tokens, one token per lane, beside the batch's last collapse
+      // (fused) post + Sinkhorn per batch of tokens, one token per lane,
+      // beside the batch's last collapse
       const int b = k % BATCH;
-      if (lane < MIX) {
-        const float mix = __fmul_rn(tot_s[lane], rstd);
-        mix_s[b][lane] = mix;
-        if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
-        if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
-        if (p.pre_out && lane < HC)
-          p.pre_out[(size_t)t * HC + lane] =
-              __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
-      }
-      __syncwarp();
       if (p.post_out && (b == BATCH - 1 || k == n_tok - 1)) {
         const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
         if (lane <= b) post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
@@ -240,10 +244,7 @@ __global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slot
       // 3. collapse into the slot (c over stream 0), sum of squares of c
       float pre[HC];
 #pragma unroll
-      for (int j = 0; j < HC; ++j) {
-        const float z = __fadd_rn(__fmul_rn(__fmul_rn(tot_s[j], rstd), p.scale[0]), p.base[j]);
-        pre[j] = __fadd_rn(sigmoid(z), p.hc_eps);
-      }
+      for (int j = 0; j < HC; ++j) pre[j] = pre_s[j];
       uint16_t *sv = reinterpret_cast<uint16_t *>(slot);
       float ssq = 0.f;
 #pragma unroll 2
