@@ -346,18 +346,15 @@ __global__ void __launch_bounds__(NT, 1)
   pdl_launch_dependents();
 
   // Stage `n` (unit n / 4, stage n % 4) into ring slot n % nslot; called by
-  // the whole producer warp, one lane issues.  The partials and streams are
-  // read once: they leave L2 first, so that residual_out (which the finish
-  // kernel reads back) stays there longest.
-  const uint64_t read_once = tc::policy_evict_first();
+  // the whole producer warp, one lane issues.
   auto fill = [&](int n) {
     const int u = u_begin + n / NSTAGE, q = n % NSTAGE;
     const int h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT + q * QT, s = n % nslot;
     unsigned char *st = ring + s * sbytes;
     if (tc::elect_one()) {
       tc::mbar_arrive_expect_tx(&full[s], uint32_t(sbytes));
-      tc::tma_load_3d_hint(st, &tm_part, h0, t0, 0, &full[s], read_once);
-      tc::tma_load_3d_hint(st + slot_res(p.tp), &tm_res, h0, 0, t0, &full[s], read_once);
+      tc::tma_load_3d(st, &tm_part, h0, t0, 0, &full[s]);
+      tc::tma_load_3d(st + slot_res(p.tp), &tm_res, h0, 0, t0, &full[s]);
       tc::tma_load_2d(st + slot_post(p.tp), &tm_post, 0, t0, &full[s]);
       tc::tma_load_2d(st + slot_comb(p.tp), &tm_comb, 0, t0, &full[s]);
     }
@@ -449,7 +446,6 @@ __global__ void __launch_bounds__(NT, 1)
     if (nm > 0) tc::mbar_wait_bounded(&mma_bar[(nm - 1) & 1], uint32_t(((nm - 1) >> 1) & 1), WAIT_LIMIT);
     __syncwarp();
   } else {
-    const uint64_t keep = tc::policy_evict_last();   // residual_out: read back by the finish kernel
     const int q = warp / STAGE_WARPS, item = (warp % STAGE_WARPS) * 32 + lane;
     const int tl = item / FRAGS, f = item % FRAGS;
     Epi ep = {p.part, p.part_stride, p.m, tmem, mma_bar, abort_s, -1, 0, 0};
@@ -493,7 +489,7 @@ __global__ void __launch_bounds__(NT, 1)
       if (t < p.m && h < p.hidden) {
         if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
 #pragma unroll
-        for (int j = 0; j < HC; ++j) tc::st_hint(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j], keep);
+        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
       }
       // the A buffer is free once the previous unit's MMAs are done
       if (ep.i >= 0) epilogue(ep);
