@@ -47,7 +47,7 @@ constexpr int CT = CWARPS * 32;                // collapse threads
 constexpr int MIX_WARP = CWARPS;               // the mixes warp
 constexpr int MAX_SLOTS = 2;
 constexpr int BATCH = 32;                      // tokens per lane-parallel Sinkhorn batch
-constexpr size_t SMEM_BUDGET = 110 * 1024;     // ring bytes of one CTA: two CTAs fit an SM
+constexpr size_t SMEM_SM = 220 * 1024;         // ring bytes of all CTAs of an SM (of 228 KB)
 constexpr size_t SMEM_LIMIT = 200 * 1024;      // one slot at H = 16384 is 133 KB
 constexpr uint32_t WAIT_LIMIT = 1u << 22;      // polls before a wait gives up
 static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collapse threads");
@@ -56,9 +56,17 @@ static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collaps
 __host__ __device__ inline size_t slot_bytes(int hidden, int part_stride) {
   return size_t(HC) * hidden * 2 + size_t(part_stride) * 4;
 }
-inline int ring_slots(int hidden, int part_stride) {
-  const size_t n = SMEM_BUDGET / slot_bytes(hidden, part_stride);
-  return n < 1 ? 1 : n > size_t(MAX_SLOTS) ? MAX_SLOTS : int(n);
+// CTAs per SM (up to 3) and ring slots per CTA: as many CTAs as fit with one
+// slot each (more warps to hide each token's latency), then a second slot.
+struct Occupancy {
+  int ctas, slots;
+};
+inline Occupancy occupancy(int hidden, int part_stride) {
+  const size_t slot = slot_bytes(hidden, part_stride);
+  int ctas = int(SMEM_SM / slot);
+  ctas = ctas < 1 ? 1 : ctas > 3 ? 3 : ctas;
+  const int slots = ctas * 2 * slot <= SMEM_SM ? 2 : 1;
+  return {ctas, slots};
 }
 
 __device__ __forceinline__ float sigmoid(float z) {
@@ -163,7 +171,7 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
   for (int i = 0; i < HC * HC; ++i) dst[i] = c[i];
 }
 
-__global__ void __launch_bounds__(NT, 2) k_finish(const FinishParams p, int slots) {
+__global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[MAX_SLOTS];
   __shared__ float pre_s[HC];
@@ -338,12 +346,11 @@ cudaError_t finish_set_attributes() {
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl) {
   if (p.hidden % VEC || p.hidden > MAX_HIDDEN || p.part_stride % 4 || p.part_stride < p.slices * VALUES)
     return cudaErrorInvalidValue;
-  const int slots = ring_slots(p.hidden, p.part_stride);
+  const Occupancy occ = occupancy(p.hidden, p.part_stride);
+  const int slots = occ.slots;
   const size_t smem = size_t(slots) * slot_bytes(p.hidden, p.part_stride);
   if (smem > SMEM_LIMIT) return cudaErrorInvalidValue;
-  // two CTAs an SM when their rings fit beside each other (227 KB an SM)
-  const int per_sm = smem <= SMEM_BUDGET ? 2 : 1;
-  const int grid = ctas * per_sm;
+  const int grid = ctas * occ.ctas;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.m < grid ? p.m : grid);
   cfg.blockDim = dim3(NT);
