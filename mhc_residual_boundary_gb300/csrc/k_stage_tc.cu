@@ -453,24 +453,6 @@ __global__ void __launch_bounds__(NT, 1)
     for (int i = 0; i < n_units; ++i) {
       if (*abort_s) break;
       const int u = u_begin + i, g = u / n_tiles, tile = u % n_tiles;
-      if (g != cur_group) {
-        // B and the A space change: the previous unit's MMAs must be done
-        if (ep.i >= 0) epilogue(ep);
-        ep.i = -1;
-        if (cur_group >= 0 && warp == 0) {
-          if (tc::elect_one()) stage_hc_fn(p, g, a_s, bfull);
-          __syncwarp();
-        }
-        if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
-          *abort_s = 1;
-          break;
-        }
-        ++loads;
-        convert_b(reinterpret_cast<const float *>(a_s), group_rows(p.hidden, g), b_s);
-        // every mixer has read the staged rows before any A row is written
-        asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
-        cur_group = g;
-      }
       const int n = i * NSTAGE + q, s = n % nslot;
       if (!tc::mbar_wait_bounded(&full[s], uint32_t((n / nslot) & 1), WAIT_LIMIT)) {
         *abort_s = 1;
@@ -493,6 +475,25 @@ __global__ void __launch_bounds__(NT, 1)
       }
       // the A buffer is free once the previous unit's MMAs are done
       if (ep.i >= 0) epilogue(ep);
+      ep.i = -1;
+      if (g != cur_group) {
+        // B and the A space change (the previous unit's MMAs are done); the
+        // first group's rows were staged at kernel start, so their split
+        // overlaps the first unit's loads and post-mix
+        if (cur_group >= 0 && warp == 0) {
+          if (tc::elect_one()) stage_hc_fn(p, g, a_s, bfull);
+          __syncwarp();
+        }
+        if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
+          *abort_s = 1;
+          break;
+        }
+        ++loads;
+        convert_b(reinterpret_cast<const float *>(a_s), group_rows(p.hidden, g), b_s);
+        // every mixer has read the staged rows before any A row is written
+        asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
+        cur_group = g;
+      }
 #pragma unroll
       for (int j = 0; j < HC; ++j) {
         const int row = 32 * q + 4 * tl + j;
