@@ -25,11 +25,10 @@
 // shared memory allows, each taking tokens blockIdx.x, blockIdx.x + gridDim.x,
 // ...  A token's four new streams are one contiguous 8H-byte run of
 // residual_out and its partial sums one 16-byte-padded row, so each token
-// arrives in shared memory by two bulk copies into a two-slot ring; thread 0
-// refills a slot as soon as the token in it is done, so the next token's
-// copies are in flight while this one is normalised and stored.  The collapse
-// keeps c in the slot (over stream 0, which the same thread has just read), so
-// the fragment loops are plain runtime loops.  Every wait is bounded; a wait
+// arrives in shared memory by two bulk copies into a ring of one or two
+// slots; the collapse keeps c in registers (BF16), so thread 0 refills the
+// slot as soon as the collapse has read it and the next token's copies are in
+// flight while this one is normalised and stored.  Every wait is bounded; a wait
 // that gives up sets bit 1 of the error word.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
@@ -171,6 +170,8 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
   for (int i = 0; i < HC * HC; ++i) dst[i] = c[i];
 }
 
+// NF: 16-byte fragments of a row per collapse thread (ceil(H / 8 / 224)).
+template <int NF>
 __global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[MAX_SLOTS];
@@ -249,45 +250,55 @@ __global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slot
         __syncwarp();
       }
     } else {
-      // 3. collapse into the slot (c over stream 0), sum of squares of c
+      // 3. collapse, kept in registers as BF16; sum of squares of c
       float pre[HC];
 #pragma unroll
       for (int j = 0; j < HC; ++j) pre[j] = pre_s[j];
-      uint16_t *sv = reinterpret_cast<uint16_t *>(slot);
+      const uint16_t *sv = reinterpret_cast<const uint16_t *>(slot);
+      uint4 cfr[NF];
       float ssq = 0.f;
-#pragma unroll 2
-      for (int fr = tid; fr < nfrag; fr += CT) {
-        float n0[8], n1[8], n2[8], n3[8], c[8];
-        uint16_t *s = sv + (size_t)fr * VEC;
-        unpack8(*reinterpret_cast<const uint4 *>(s), n0);
-        unpack8(*reinterpret_cast<const uint4 *>(s + H), n1);
-        unpack8(*reinterpret_cast<const uint4 *>(s + 2 * H), n2);
-        unpack8(*reinterpret_cast<const uint4 *>(s + 3 * H), n3);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], pre[0]), __fmul_rn(n1[e], pre[1])),
-                           __fadd_rn(__fmul_rn(n2[e], pre[2]), __fmul_rn(n3[e], pre[3])));
-        *reinterpret_cast<uint4 *>(s) = round8(c);
+      for (int i = 0; i < NF; ++i) {
+        const int fr = tid + i * CT;
+        cfr[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (fr < nfrag) {
+          float n0[8], n1[8], n2[8], n3[8], c[8];
+          const uint16_t *s = sv + (size_t)fr * VEC;
+          unpack8(*reinterpret_cast<const uint4 *>(s), n0);
+          unpack8(*reinterpret_cast<const uint4 *>(s + H), n1);
+          unpack8(*reinterpret_cast<const uint4 *>(s + 2 * H), n2);
+          unpack8(*reinterpret_cast<const uint4 *>(s + 3 * H), n3);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
+          for (int e = 0; e < 8; ++e)
+            c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], pre[0]), __fmul_rn(n1[e], pre[1])),
+                             __fadd_rn(__fmul_rn(n2[e], pre[2]), __fmul_rn(n3[e], pre[3])));
+          cfr[i] = round8(c);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
+        }
       }
       ssq = warp_sum(ssq);
       if (lane == 0) red_s[warp] = ssq;
+      // the slot's next fill is an async-proxy write after these generic reads
+      tc::fence_proxy_async_smem();
       asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
+      // the slot has been read: it takes the token `slots` places further on,
+      // whose copies then overlap this token's normalisation
+      if (tid == 0 && filled < n_tok) fill(filled++);
       float sq = 0.f;
 #pragma unroll
       for (int w = 0; w < CWARPS; ++w) sq += red_s[w];
       const float ir = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(sq, float(H)), p.norm_eps)));
 
       // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
-#pragma unroll 2
-      for (int base = 0; base < nfrag; base += CT) {
-        const int fr = base + tid;
+#pragma unroll
+      for (int i = 0; i < NF; ++i) {
+        const int fr = tid + i * CT;
         const bool live = fr < nfrag;
         float o[8];
         if (live) {
           float c[8], g[8];
-          unpack8(*reinterpret_cast<const uint4 *>(sv + (size_t)fr * VEC), c);
+          unpack8(cfr[i], c);
           unpack8(ld_vec(p.gamma + (size_t)fr * VEC), g);
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(c[e], ir), g[e]);
@@ -314,11 +325,7 @@ __global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slot
         }
       }
     }
-    // the slot's next fill is an async-proxy write after these generic accesses
-    tc::fence_proxy_async_smem();
     __syncthreads();
-    // the slot is done: it takes the token `slots` places further on
-    if (tid == 0 && filled < n_tok) fill(filled++);
   }
   pdl_launch_dependents();
 
@@ -339,8 +346,18 @@ __global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slot
 
 }  // namespace
 
+constexpr int NFMAX = (MAX_HIDDEN / VEC + CT - 1) / CT;
+static_assert(NFMAX == 10, "launch_finish dispatches NF = 1 .. 10");
+using FinishKernel = void (*)(FinishParams, int);
+constexpr FinishKernel kFinish[NFMAX] = {k_finish<1>, k_finish<2>, k_finish<3>, k_finish<4>, k_finish<5>,
+                                         k_finish<6>, k_finish<7>, k_finish<8>, k_finish<9>, k_finish<10>};
+
 cudaError_t finish_set_attributes() {
-  return cudaFuncSetAttribute(k_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+  for (FinishKernel k : kFinish) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_LIMIT));
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl) {
@@ -361,7 +378,8 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_finish, p, slots);
+  const int nf = (p.hidden / VEC + CT - 1) / CT;
+  return cudaLaunchKernelEx(&cfg, kFinish[nf - 1], p, slots);
 }
 
 }  // namespace mhc
