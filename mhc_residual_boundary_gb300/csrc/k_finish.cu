@@ -33,6 +33,8 @@
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
+#include <atomic>
+
 #include "device_common.cuh"
 #include "launch.cuh"
 #include "tcgen05.cuh"
@@ -46,7 +48,7 @@ constexpr int CT = CWARPS * 32;                // collapse threads
 constexpr int MIX_WARP = CWARPS;               // the mixes warp
 constexpr int MAX_SLOTS = 2;
 constexpr int BATCH = 32;                      // tokens per lane-parallel Sinkhorn batch
-constexpr size_t SMEM_SM = 220 * 1024;         // ring bytes of all CTAs of an SM (of 228 KB)
+constexpr size_t SMEM_SM = 216 * 1024;         // ring bytes of all CTAs of an SM (of 228 KB)
 constexpr size_t SMEM_LIMIT = 200 * 1024;      // one slot at H = 16384 is 133 KB
 constexpr uint32_t WAIT_LIMIT = 1u << 22;      // polls before a wait gives up
 static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collapse threads");
@@ -55,15 +57,15 @@ static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collaps
 __host__ __device__ inline size_t slot_bytes(int hidden, int part_stride) {
   return size_t(HC) * hidden * 2 + size_t(part_stride) * 4;
 }
-// CTAs per SM (up to 3) and ring slots per CTA: as many CTAs as fit with one
-// slot each (more warps to hide each token's latency), then a second slot.
+// CTAs per SM (up to 4) and ring slots per CTA: as many CTAs as fit with one
+// slot each (more warps and more tokens in flight), then a second slot.
 struct Occupancy {
   int ctas, slots;
 };
 inline Occupancy occupancy(int hidden, int part_stride) {
   const size_t slot = slot_bytes(hidden, part_stride);
   int ctas = int(SMEM_SM / slot);
-  ctas = ctas < 1 ? 1 : ctas > 3 ? 3 : ctas;
+  ctas = ctas < 1 ? 1 : ctas > 4 ? 4 : ctas;
   const int slots = ctas * 2 * slot <= SMEM_SM ? 2 : 1;
   return {ctas, slots};
 }
@@ -172,7 +174,7 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
 
 // NF: 16-byte fragments of a row per collapse thread (ceil(H / 8 / 224)).
 template <int NF>
-__global__ void __launch_bounds__(NT, 3) k_finish(const FinishParams p, int slots) {
+__global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[MAX_SLOTS];
   __shared__ float pre_s[HC];
@@ -367,7 +369,22 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
   const int slots = occ.slots;
   const size_t smem = size_t(slots) * slot_bytes(p.hidden, p.part_stride);
   if (smem > SMEM_LIMIT) return cudaErrorInvalidValue;
-  const int grid = ctas * occ.ctas;
+  const int nf = (p.hidden / VEC + CT - 1) / CT;
+  // persistent: as many CTAs as are resident at once (the runtime's count, so
+  // that the static shared memory and the per-CTA reservation are included)
+  // (cached per kernel and ring size: the query costs host time on every call)
+  static std::atomic<uint64_t> cache[NFMAX];
+  const uint64_t cached = cache[nf - 1].load(std::memory_order_relaxed);
+  int resident = 0;
+  if (cached && (cached >> 8) == smem) {
+    resident = int(cached & 0xff);
+  } else {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kFinish[nf - 1], NT, smem);
+    if (e != cudaSuccess) return e;
+    cache[nf - 1].store((uint64_t(smem) << 8) | uint64_t(resident & 0xff), std::memory_order_relaxed);
+  }
+  resident = resident < 1 ? 1 : resident > occ.ctas ? occ.ctas : resident;
+  const int grid = ctas * resident;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.m < grid ? p.m : grid);
   cfg.blockDim = dim3(NT);
@@ -378,7 +395,6 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  const int nf = (p.hidden / VEC + CT - 1) / CT;
   return cudaLaunchKernelEx(&cfg, kFinish[nf - 1], p, slots);
 }
 
