@@ -134,9 +134,9 @@ def measured_peaks():
 def kernel_traffic(w):
     """dram bytes per launch of the stage kernel from the committed ncu
     summary, only if it was taken on this workload with the current source."""
-    src = os.path.join(ROOT, "mhc_residual_boundary_gb300", "csrc", "k_stage.cu")
+    src = os.path.join(ROOT, "mhc_residual_boundary_gb300", "csrc", "k_stage_tc.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:12]
-    pat = re.compile(r"traffic: workload=(\S+) tokens=(\d+) kernel=k_stage source_sha=(\w+) "
+    pat = re.compile(r"traffic: workload=(\S+) tokens=(\d+) kernel=k_stage_tc source_sha=(\w+) "
                      r"bytes_per_launch=(\d+)")
     pdir = os.path.join(ROOT, "profiles")
     for name in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
@@ -326,7 +326,7 @@ def run_ours(args, w):
     stage_ms = prof["stage_ms"] / max(prof["calls"], 1)
     achieved = nbytes["stage"] / (stage_ms * 1e-3) / 1e9
     call_gbs = nbytes["total"] / (ms_per_step * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "k_stage", "achieved": achieved, "peak": peak, "unit": "GB/s",
+    roofline = {"bound": "hbm", "kernel": "k_stage_tc", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": kernel_traffic(w),
                 "algorithmic_bytes_per_launch": nbytes["stage"], "avg_launch_ms": stage_ms,
                 "peak_source": peak_src,

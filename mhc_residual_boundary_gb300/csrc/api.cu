@@ -1,12 +1,14 @@
 // api.cu -- host implementation of include/mhc_boundary.h.
 //
-// Call structure ([GLM] AllReduceMhcBoundary.__call__ / join): the caller's
-// stream first waits for the previous call's side kernel; the stage kernel
-// and the finish kernel (programmatic dependent launch) run on the caller's
-// stream; an event then lets the side stream run the post / Sinkhorn kernel,
-// whose completion event the next call (or join) waits for.  Every argument
-// is validated before the first launch and a failing call leaves the handle
-// unchanged ([DSV] AllReduceMHC._consumer).
+// Call structure ([GLM] AllReduceMhcBoundary.__call__ / join): on the
+// caller's stream, the MoE fold kernel (finalize_moe only), the stage kernel
+// and the finish kernel (programmatic dependent launch), which also computes
+// post and the Sinkhorn mix.  With MHC_FLAG_SIDE_MIXES the post / Sinkhorn
+// kernel runs instead on a library side stream after an event; the next call
+// (or join) waits for its completion event.  With MHC_FLAG_SYNC_MIXES that
+// kernel runs on the caller's stream.  Every argument is validated before the
+// first launch and a failing call leaves the handle unchanged ([DSV]
+// AllReduceMHC._consumer).
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
