@@ -111,5 +111,11 @@ def make_inputs(hidden: int, tp: int, m: int, *, top_k: int = 0, moe: bool = Fal
     return out
 
 
+def bf16_weight(hc_fn: np.ndarray) -> np.ndarray:
+    """The prenorm weight in the GLM page's form, BF16 [24][4H], from the FP32
+    [4H][24] draw (the same values, transposed and rounded to BF16)."""
+    return bf16_bits(np.ascontiguousarray(hc_fn.T))
+
+
 def inputs_for(w: Workload, seed: int = 0) -> dict:
     return make_inputs(w.hidden, w.tp, w.m, top_k=w.top_k, moe=w.moe, seed=seed)

@@ -73,7 +73,7 @@ class OracleConfig(ctypes.Structure):
 class OracleIO(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "partials", "routed", "idx", "weights", "shared", "residual", "post",
-        "comb", "hc_fn", "scale", "base", "gamma", "residual_out",
+        "comb", "hc_fn", "hc_fn_bf16", "scale", "base", "gamma", "residual_out",
         "layer_input", "post_out", "comb_out", "mixes", "pre", "reduced",
         "mx_values", "mx_scales")]
 
@@ -96,7 +96,7 @@ def _load():
             getattr(lib, name).restype = None
         steps = {
             "oracle_stage1": 2, "oracle_moe_fold": 5, "oracle_post_mix": 5,
-            "oracle_prenorm_gemv": 4, "oracle_mixes_and_pre": 6,
+            "oracle_prenorm_gemv": 4, "oracle_prenorm_gemv_bf16": 4, "oracle_mixes_and_pre": 6,
             "oracle_post_from_mixes": 4, "oracle_sinkhorn": 4,
             "oracle_collapse_norm": 4,
         }
@@ -235,6 +235,18 @@ def prenorm_gemv(streams, hc_fn):
     return raw, ss
 
 
+def prenorm_gemv_bf16(streams, fn):
+    """The GEMV with the weight as BF16 [24][4H] (the GLM page's layout)."""
+    m, _, hidden = streams.shape
+    streams = _arr(streams, np.uint16)
+    fn = _arr(fn, np.uint16, (MIX, HC * hidden))
+    raw = np.zeros((m, MIX), np.float32)
+    ss = np.zeros((m,), np.float32)
+    cfg = Problem(hidden, 1, m).c()
+    _load().oracle_prenorm_gemv_bf16(ctypes.byref(cfg), 0, m, _p(streams), _p(fn), _p(raw), _p(ss))
+    return raw, ss
+
+
 def mixes_and_pre(raw, ss, scale, base, hidden, rms_eps=1e-6, hc_eps=1e-6):
     m = raw.shape[0]
     raw = _arr(raw, np.float32, (m, MIX))
@@ -327,6 +339,7 @@ def boundary(problem: Problem, inputs: dict, *, moe: bool = False,
     for name, dtype in (("partials", np.uint16), ("routed", np.uint16), ("idx", np.int32),
                         ("weights", np.float32), ("shared", np.uint16), ("residual", np.uint16),
                         ("post", np.float32), ("comb", np.float32), ("hc_fn", np.float32),
+                        ("hc_fn_bf16", np.uint16),
                         ("scale", np.float32), ("base", np.float32), ("gamma", np.uint16)):
         setattr(io, name, ptr(name, dtype, inputs))
     for name in ("residual_out", "layer_input", "post_out", "comb_out", "mixes", "pre",

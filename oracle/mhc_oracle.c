@@ -233,6 +233,32 @@ void oracle_prenorm_gemv(const oracle_config_t *c, int32_t t0, int32_t t1,
   }
 }
 
+void oracle_prenorm_gemv_bf16(const oracle_config_t *c, int32_t t0, int32_t t1,
+                              const uint16_t *streams, const uint16_t *fn,
+                              float *raw, float *sum_squares) {
+  /* The same 24 dot products with the weight as the GLM page passes it
+   * ([GLM] AllReduceMhcBoundary.__call__, fn: [24, hc * hidden] BF16;
+   * _BoundaryDeviceKernel.kernel reads element row * (hc * hidden) +
+   * lane * hidden + column, i.e. output i, stream j, column h at
+   * i * 4H + j * H + h).  Each BF16 x BF16 product is exact; the sums are
+   * taken in FP64 and rounded once, as for the FP32 weight. */
+  const size_t H = (size_t)c->hidden;
+  for (int32_t t = t0; t < t1; ++t) {
+    double acc[MIX];
+    double squares = 0.0;
+    for (int i = 0; i < MIX; ++i) acc[i] = 0.0;
+    for (int j = 0; j < HC; ++j) {
+      for (size_t h = 0; h < H; ++h) {
+        double v = (double)BF(streams[((size_t)t * HC + j) * H + h]);
+        for (int i = 0; i < MIX; ++i) acc[i] += (double)BF(fn[(size_t)i * HC * H + (size_t)j * H + h]) * v;
+        squares += v * v;
+      }
+    }
+    for (int i = 0; i < MIX; ++i) raw[(size_t)t * MIX + i] = (float)acc[i];
+    sum_squares[t] = (float)squares;
+  }
+}
+
 static float sigmoid_f32(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 void oracle_mixes_and_pre(const oracle_config_t *c, int32_t t0, int32_t t1,
@@ -398,7 +424,10 @@ int oracle_boundary(const oracle_config_t *c, int32_t t0, int32_t t1, int moe,
     else
       oracle_stage1(c, t0, t1, io->partials, y);
     oracle_post_mix(c, t0, t1, y, io->residual, io->post, io->comb, io->residual_out);
-    oracle_prenorm_gemv(c, t0, t1, io->residual_out, io->hc_fn, raw, ss);
+    if (io->hc_fn_bf16)
+      oracle_prenorm_gemv_bf16(c, t0, t1, io->residual_out, io->hc_fn_bf16, raw, ss);
+    else
+      oracle_prenorm_gemv(c, t0, t1, io->residual_out, io->hc_fn, raw, ss);
     oracle_mixes_and_pre(c, t0, t1, raw, ss, io->scale, io->base, mixes, pre);
     oracle_collapse_norm(c, t0, t1, io->residual_out, pre, io->gamma, io->layer_input);
     oracle_post_from_mixes(c, t0, t1, mixes, io->scale, io->base, io->post_out);

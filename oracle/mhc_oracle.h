@@ -78,6 +78,11 @@ void oracle_post_mix(const oracle_config_t *c, int32_t t0, int32_t t1,
 void oracle_prenorm_gemv(const oracle_config_t *c, int32_t t0, int32_t t1,
                          const uint16_t *streams, const float *hc_fn,
                          float *raw, float *sum_squares);
+/* The same with the weight in the GLM page's form: fn [24][4H] BF16, output i,
+ * stream j, column h at i * 4H + j * H + h. */
+void oracle_prenorm_gemv_bf16(const oracle_config_t *c, int32_t t0, int32_t t1,
+                              const uint16_t *streams, const uint16_t *fn,
+                              float *raw, float *sum_squares);
 void oracle_mixes_and_pre(const oracle_config_t *c, int32_t t0, int32_t t1,
                           const float *raw, const float *sum_squares,
                           const float *scale, const float *base,
@@ -111,6 +116,7 @@ typedef struct {
   const float *post;
   const float *comb;
   const float *hc_fn;
+  const uint16_t *hc_fn_bf16; /* [24][4H] bf16; used instead of hc_fn when set */
   const float *scale;
   const float *base;
   const uint16_t *gamma;

@@ -195,6 +195,33 @@ def test_gemv_matches_float64_matmul(oracle_lib):
     assert np.allclose(ss, np.einsum("ij,ij->i", flat, flat), rtol=1e-6)
 
 
+def test_gemv_bf16_weight_one_hot_pins_its_layout(oracle_lib):
+    # fn is [24][4H]: a one at row i, column j*H + h selects stream j, column h
+    # for output i (a transposed or stream/column-swapped read fails)
+    hidden, m = 40, 3
+    inp = synth.make_inputs(hidden, 1, m, seed=8)
+    streams = inp["residual"]
+    for j, h, i in ((0, 0, 0), (3, 39, 23), (2, 17, 5), (1, 5, 12)):
+        fn = np.zeros((MIX, HC * hidden), np.uint16)
+        fn[i, j * hidden + h] = 0x3F80          # BF16 1.0
+        raw, _ = oracle_lib.prenorm_gemv_bf16(streams, fn)
+        assert np.array_equal(raw[:, i], f32(streams[:, j, h]))
+        assert (np.delete(raw, i, axis=1) == 0).all()
+
+
+def test_gemv_bf16_weight_matches_float64_matmul(oracle_lib):
+    inp = synth.make_inputs(256, 1, 7, seed=9)
+    fn = bits(inp["hc_fn"].T)                    # [24][4H] BF16
+    raw, ss = oracle_lib.prenorm_gemv_bf16(inp["residual"], fn)
+    flat = f32(inp["residual"]).reshape(7, -1).astype(np.float64)
+    ref = np.matmul(flat, f32(fn).astype(np.float64).T)
+    assert np.allclose(raw, ref, rtol=1e-6, atol=1e-6)
+    assert np.allclose(ss, np.einsum("ij,ij->i", flat, flat), rtol=1e-6)
+    # the same weights widened to FP32 [4H][24] give the same bits
+    raw32, ss32 = oracle_lib.prenorm_gemv(inp["residual"], np.ascontiguousarray(f32(fn).T))
+    assert np.array_equal(raw, raw32) and np.array_equal(ss, ss32)
+
+
 def test_mixes_rms_uses_all_four_streams(oracle_lib):
     # new = c everywhere, fn one-hot: raw = c, ss = 4H c^2, so
     # mixes = c / sqrt(c^2 + eps): +-1 up to eps, whatever H and c.
