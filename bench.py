@@ -62,7 +62,7 @@ def workload(name, m):
     w = cands[-1] if m is None else next((c for c in cands if c.m == m), None)
     if w is None:
         base = cands[-1]
-        w = synth.Workload(base.name, base.hidden, base.tp, m, base.top_k, base.moe, base.mxfp8)
+        w = synth.Workload(base.name, base.hidden, base.tp, m, base.top_k, base.moe, base.mxfp8, base.bf16_fn)
     return w
 
 
@@ -74,7 +74,7 @@ def call_bytes(w):
         stage1 = tp * K * 2 * H + tp * 2 * H + tp * K * 4 + K * 4
     else:
         stage1 = 2 * tp * H
-    stage = M * (stage1 + 8 * H + 8 * H + 16 + 64) + 4 * H * 24 * 4
+    stage = M * (stage1 + 8 * H + 8 * H + 16 + 64) + 4 * H * 24 * (2 if w.bf16_fn else 4)
     finish = 2 * H + M * 2 * H
     if w.mxfp8:
         padded = (M + 127) // 128 * 128
@@ -85,7 +85,8 @@ def call_bytes(w):
 
 def describe(w):
     return {"workload": w.name, "tokens": w.m, "hidden": w.hidden, "tp": w.tp, "hc": 4,
-            "top_k": w.top_k, "moe": w.moe, "mxfp8": w.mxfp8}
+            "top_k": w.top_k, "moe": w.moe, "mxfp8": w.mxfp8,
+            "weight": "bf16 [24][4H]" if w.bf16_fn else "f32 [4H][24]"}
 
 
 # ------------------------------------------------------------------ ranks
@@ -339,7 +340,7 @@ def run_ours(args, w):
     e2e = None
     if not w.moe and args.e2e_steps > 0:
         host_in = {k: v.cpu().pin_memory() for k, v in dev_in.items() if k in (
-            "partials", "residual", "post", "comb", "hc_fn", "scale", "base", "norm_weight")}
+            "partials", "residual", "post", "comb", "hc_fn", "hc_fn_bf16", "scale", "base", "norm_weight")}
         host_out = b.empty_outputs(w.m, mxfp8=w.mxfp8, device="cpu", pin_memory=True)
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())

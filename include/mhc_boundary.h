@@ -113,6 +113,7 @@ typedef struct mhc_boundary mhc_boundary_t; /* opaque, library-owned */
  *   post        [m][4]     f32 : post-mix of the previous boundary
  *   comb        [m][4][4]  f32 : residual mix, indexed [source][target]
  *   hc_fn       [4H][24]   f32 : prenorm GEMV weight, row j*H + h
+ *                                  (or NULL when hc_fn_bf16 is given)
  *   scale       [3]        f32 : mix scales (pre, post, comb)
  *   base        [24]       f32 : mix biases (pre 0..3, post 4..7, comb 8..23)
  *   norm_weight [H]        bf16: RMSNorm weight
@@ -147,6 +148,11 @@ typedef struct {
   void *reduced_out;
   uint8_t *mxfp8_values;
   uint8_t *mxfp8_scales;
+  /* The prenorm weight in the GLM page's form instead of hc_fn ([GLM]
+   * AllReduceMhcBoundary.__call__, fn): [24][4H] bf16, output i, stream j,
+   * column h at i*4H + j*H + h.  Exactly one of hc_fn and hc_fn_bf16 is
+   * non-NULL; hc_fn_bf16 needs tp <= 8 (MHC_ERR_UNSUPPORTED otherwise). */
+  const void *hc_fn_bf16;
 } mhc_run_args_t;
 
 /* Arguments of a boundary call whose stage 1 folds an unfinalised MoE output

@@ -23,6 +23,7 @@ INPUT_SPECS = {
     "post": (torch.float32, lambda tp, m, H, K, R: (m, HC)),
     "comb": (torch.float32, lambda tp, m, H, K, R: (m, HC, HC)),
     "hc_fn": (torch.float32, lambda tp, m, H, K, R: (HC * H, MIX)),
+    "hc_fn_bf16": (torch.bfloat16, lambda tp, m, H, K, R: (MIX, HC * H)),
     "scale": (torch.float32, lambda tp, m, H, K, R: (3,)),
     "base": (torch.float32, lambda tp, m, H, K, R: (MIX,)),
     "norm_weight": (torch.bfloat16, lambda tp, m, H, K, R: (H,)),
@@ -113,7 +114,9 @@ class Boundary:
         rows = inputs["routed"].shape[1] if moe else 0
         args = capi.mhc_run_args_t()
         args.m = m
-        names = ["residual", "post", "comb", "hc_fn", "scale", "base", "norm_weight"]
+        # the prenorm weight: FP32 [4H][24] (hc_fn) or BF16 [24][4H] (hc_fn_bf16)
+        weight = "hc_fn_bf16" if inputs.get("hc_fn_bf16") is not None else "hc_fn"
+        names = ["residual", "post", "comb", weight, "scale", "base", "norm_weight"]
         names += ["routed", "idx", "weights", "shared"] if moe else ["partials"]
         for n in names:
             t = inputs[n]

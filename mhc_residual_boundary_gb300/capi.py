@@ -38,7 +38,7 @@ class mhc_boundary_config_t(ctypes.Structure):
 
 RUN_FIELDS = ("partials", "residual", "post", "comb", "hc_fn", "scale", "base", "norm_weight",
               "residual_out", "layer_input", "post_out", "comb_out", "pre_out", "mixes_out",
-              "reduced_out", "mxfp8_values", "mxfp8_scales")
+              "reduced_out", "mxfp8_values", "mxfp8_scales", "hc_fn_bf16")
 
 
 class mhc_run_args_t(ctypes.Structure):

@@ -92,7 +92,7 @@ mhc_status_t validate(const mhc_boundary *b, const mhc_run_args_t *a, bool moe, 
   struct Need { const void *p; const char *name; size_t align; };
   const Need required[] = {
       {a->residual, "residual", 16}, {a->post, "post", 16}, {a->comb, "comb", 16},
-      {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
+      {a->scale, "scale", 4}, {a->base, "base", 4},
       {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
       {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4},
       {a->comb_out, "comb_out", 4}};
@@ -101,6 +101,12 @@ mhc_status_t validate(const mhc_boundary *b, const mhc_run_args_t *a, bool moe, 
     if (!aligned(n.p, n.align))
       return fail(msg, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
   }
+  if ((a->hc_fn == nullptr) == (a->hc_fn_bf16 == nullptr))
+    return fail(msg, MHC_ERR_INVALID_ARG, "exactly one of hc_fn and hc_fn_bf16 is required");
+  if (!aligned(a->hc_fn ? static_cast<const void *>(a->hc_fn) : a->hc_fn_bf16, 16))
+    return fail(msg, MHC_ERR_INVALID_ARG, "the prenorm weight is not 16-byte aligned");
+  if (a->hc_fn_bf16 && !moe && c.tp > TP_TMA_MAX)
+    return fail(msg, MHC_ERR_UNSUPPORTED, "hc_fn_bf16 needs tp <= %d", TP_TMA_MAX);
   if (moe) {
     if (a->partials) return fail(msg, MHC_ERR_INVALID_ARG, "partials must be NULL for finalize_moe");
   } else {
@@ -199,6 +205,8 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.post = a->post;
   sp.comb = a->comb;
   sp.hc_fn = a->hc_fn;
+  sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
+  sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = b->part;
@@ -457,6 +465,7 @@ mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *host
   d.post = host->post ? reinterpret_cast<float *>(base + L.post) : nullptr;
   d.comb = host->comb ? reinterpret_cast<float *>(base + L.comb) : nullptr;
   d.hc_fn = host->hc_fn ? reinterpret_cast<float *>(base + L.hc_fn) : nullptr;
+  d.hc_fn_bf16 = host->hc_fn_bf16 ? static_cast<const void *>(base + L.hc_fn) : nullptr;
   d.scale = host->scale ? reinterpret_cast<float *>(base + L.scale) : nullptr;
   d.base = host->base ? reinterpret_cast<float *>(base + L.base) : nullptr;
   d.norm_weight = host->norm_weight ? base + L.gamma : nullptr;
@@ -483,7 +492,8 @@ mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *host
       {base + L.residual, host->residual, M * HC * H * 2},
       {base + L.post, host->post, M * HC * 4},
       {base + L.comb, host->comb, M * HC * HC * 4},
-      {base + L.hc_fn, host->hc_fn, size_t(HC) * H * MIX * 4},
+      {base + L.hc_fn, host->hc_fn ? static_cast<const void *>(host->hc_fn) : host->hc_fn_bf16,
+       size_t(HC) * H * MIX * (host->hc_fn ? 4 : 2)},
       {base + L.scale, host->scale, 3 * 4},
       {base + L.base, host->base, MIX * 4},
       {base + L.gamma, host->norm_weight, H * 2}};

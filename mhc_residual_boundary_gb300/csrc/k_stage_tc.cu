@@ -75,7 +75,8 @@ constexpr int FRAGS = UK / VEC;               // 16-byte fragments per row piece
 constexpr int A_KCOL = ROWS * 16 + 16;        // bytes between A core columns (+16: fewer bank conflicts)
 constexpr int A_BYTES = KCOLS * A_KCOL;
 constexpr int B_KCOL = UN * 16;               // bytes between B core columns
-constexpr int B_BYTES = 3 * KCOLS * B_KCOL;   // hi, mid, lo
+constexpr int TERM_BYTES = KCOLS * B_KCOL;    // one BF16 term of B
+constexpr int B_BYTES = 3 * TERM_BYTES;       // FP32 weight: hi, mid, lo
 constexpr int ROW = UK * 2;                   // bytes of one 128-column BF16 row piece
 constexpr int MAX_SLOTS = 8;
 constexpr uint32_t D_STRIDE = 128;            // TMEM columns between the two accumulators
@@ -86,14 +87,17 @@ constexpr int B_PAIRS = (UK / 2) * UN / MIX_THREADS;   // hc_fn element pairs pe
 constexpr int OUTS = MIX / STAGE_WARPS;       // outputs one epilogue warp reads per block (6)
 constexpr int HC_ROWS_BYTES = UK * MIX * 4;   // one stream's hc_fn rows of a group (FP32)
 constexpr int STAGING = HC * HC_ROWS_BYTES;   // a group's hc_fn rows, staged over the A buffer
+constexpr int FN_SEG = UK * 2;                // BF16 weight: one (output, stream) row piece of a group
+constexpr int STAGING_BF16 = MIX * HC * FN_SEG;   // a group's 96 row pieces
 static_assert(QT * FRAGS == STAGE_WARPS * 32, "one item per mixer thread");
 static_assert(ROWS == 4 * 32 && QT * HC == 32, "one TMEM lane quarter per stage");
 static_assert((UK / 2) * UN % MIX_THREADS == 0 && B_PAIRS == 12, "B build split");
 static_assert(OUTS == 6, "epilogue split: four outputs plus two");
 static_assert(UK % 16 == 0 && UN % 16 == 0 && UN <= 256, "MMA shape");
 
-// Shared memory: control block, B, A (whose space also takes a group's
-// staged hc_fn rows), then the ring of stage slots.
+// Shared memory: control block, B (three BF16 terms for an FP32 weight, one
+// for a BF16 weight), A (whose space also takes a group's staged weight
+// rows), then the ring of stage slots.
 struct Layout {
   static constexpr int full = 0;                        // uint64 [MAX_SLOTS]
   static constexpr int empty = full + 8 * MAX_SLOTS;    // uint64 [MAX_SLOTS]
@@ -103,11 +107,15 @@ struct Layout {
   static constexpr int slot = bfull + 8;                // TMEM address
   static constexpr int abort = slot + 4;                // int
   static constexpr int b = 256;
-  static constexpr int a = b + B_BYTES;
-  static constexpr int ring = a + (A_BYTES > STAGING ? A_BYTES : STAGING);
   static_assert(abort + 4 <= b, "control block");
-  static_assert(a % 128 == 0 && b % 128 == 0 && ring % 128 == 0, "TMA / MMA alignment");
+  static_assert(b % 128 == 0 && TERM_BYTES % 128 == 0 && A_BYTES % 128 == 0, "TMA / MMA alignment");
 };
+__host__ __device__ constexpr int layout_a(int terms) { return Layout::b + terms * TERM_BYTES; }
+__host__ __device__ constexpr int layout_ring(int terms) {
+  return layout_a(terms) + (terms == 3 ? (A_BYTES > STAGING ? A_BYTES : STAGING)
+                                       : (A_BYTES > STAGING_BF16 ? A_BYTES : STAGING_BF16));
+}
+static_assert(layout_ring(3) % 128 == 0 && layout_ring(1) % 128 == 0, "TMA alignment");
 
 // A stage slot: partials [tp][8][128] bf16, streams [8][4][128] bf16,
 // post [8][4] f32, comb [8][16] f32 (each part 128-byte aligned).
@@ -115,12 +123,13 @@ __host__ __device__ constexpr int slot_res(int tp) { return tp * QT * ROW; }
 __host__ __device__ constexpr int slot_post(int tp) { return slot_res(tp) + QT * HC * ROW; }
 __host__ __device__ constexpr int slot_comb(int tp) { return slot_post(tp) + QT * HC * 4; }
 __host__ __device__ constexpr int slot_bytes(int tp) { return slot_comb(tp) + QT * HC * HC * 4; }
-__host__ __device__ constexpr int ring_slots(int tp) {
-  return (SMEM_MAX - Layout::ring) / slot_bytes(tp) < MAX_SLOTS ? (SMEM_MAX - Layout::ring) / slot_bytes(tp)
-                                                                 : MAX_SLOTS;
+__host__ __device__ constexpr int ring_slots(int tp, int terms) {
+  return (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) < MAX_SLOTS
+             ? (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp)
+             : MAX_SLOTS;
 }
 static_assert(slot_bytes(1) % 128 == 0 && slot_post(1) % 128 == 0 && slot_comb(1) % 128 == 0, "slot alignment");
-static_assert(ring_slots(TP_TMA_MAX) >= NSTAGE, "a unit's four stages fit the ring");
+static_assert(ring_slots(TP_TMA_MAX, 3) >= NSTAGE, "a unit's four stages fit the ring");
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 __device__ __forceinline__ float lane4(const float4 &v, int j) {
@@ -183,19 +192,60 @@ __device__ __noinline__ void convert_b(const float *stg, int rows, unsigned char
   }
 }
 
+// The BF16 weight's group: its 96 staged row pieces (output i, stream j at
+// stg + (j * 24 + i) * 256 bytes, 128 columns each; columns past `rows` are
+// zero) are already BF16, so B is their 16-byte pieces moved to the core-
+// matrix layout: piece (n, kc) of row n = j * 24 + i to core column kc.
+__device__ __noinline__ void place_b_bf16(const unsigned char *stg, int rows, unsigned char *b_s) {
+  constexpr int PIECES = UN * KCOLS;
+  static_assert(PIECES % MIX_THREADS == 0, "B placement split");
+#pragma unroll
+  for (int it = 0; it < PIECES / MIX_THREADS; ++it) {
+    const int e = threadIdx.x + it * MIX_THREADS;
+    const int kc = e % KCOLS, n = e / KCOLS;
+    const uint4 v = kc * 8 < rows ? *reinterpret_cast<const uint4 *>(stg + n * FN_SEG + kc * 16)
+                                  : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(b_s + kc * B_KCOL + (n >> 3) * 128 + (n & 7) * 16) = v;
+  }
+}
+
 // Rows of group g (at most 128; fewer in the last group).
 __device__ __forceinline__ int group_rows(int hidden, int g) {
   return hidden - g * UK < UK ? hidden - g * UK : UK;
 }
 
-// One lane: the four bulk copies of group g's hc_fn rows into `stg`, counted
-// on `bar`.
+// Group g's weight rows into `stg`, counted on `bar`; called by a whole warp.
+// FP32 weight: four bulk copies (one per stream, 128 rows of 24 floats).
+// BF16 weight: 96 bulk copies of 256-byte row pieces, three per lane.
 __device__ __forceinline__ void stage_hc_fn(const StageParams &p, int g, unsigned char *stg, uint64_t *bar) {
   const int rows = group_rows(p.hidden, g);
-  tc::mbar_arrive_expect_tx(bar, uint32_t(HC * rows * MIX * 4));
-  for (int j = 0; j < HC; ++j)
-    tc::bulk_load(stg + j * HC_ROWS_BYTES, p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX,
-                  uint32_t(rows * MIX * 4), bar);
+  if (p.fn_terms == 3) {
+    if (tc::elect_one()) {
+      tc::mbar_arrive_expect_tx(bar, uint32_t(HC * rows * MIX * 4));
+      for (int j = 0; j < HC; ++j)
+        tc::bulk_load(stg + j * HC_ROWS_BYTES, p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX,
+                      uint32_t(rows * MIX * 4), bar);
+    }
+    __syncwarp();
+  } else {
+    if (tc::elect_one()) tc::mbar_arrive_expect_tx(bar, uint32_t(MIX * HC * rows * 2));
+    __syncwarp();
+    for (int n = threadIdx.x & 31; n < MIX * HC; n += 32) {
+      const int j = n / MIX, i = n % MIX;
+      tc::bulk_load(stg + n * FN_SEG,
+                    p.hc_fn_bf16 + (size_t)i * HC * p.hidden + (size_t)j * p.hidden + (size_t)g * UK,
+                    uint32_t(rows * 2), bar);
+    }
+    __syncwarp();
+  }
+}
+
+// Splits (FP32) or places (BF16) the staged weight rows of group g into B.
+__device__ __forceinline__ void build_b(const StageParams &p, int g, const unsigned char *stg, unsigned char *b_s) {
+  if (p.fn_terms == 3)
+    convert_b(reinterpret_cast<const float *>(stg), group_rows(p.hidden, g), b_s);
+  else
+    place_b_bf16(stg, group_rows(p.hidden, g), b_s);
 }
 
 // ------------------------------------------------------------- epilogue
@@ -327,9 +377,9 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + Layout::bfull);
   uint32_t *slot = reinterpret_cast<uint32_t *>(smem + Layout::slot);
   volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Layout::abort);
-  unsigned char *a_s = smem + Layout::a;
+  unsigned char *a_s = smem + layout_a(p.fn_terms);
   unsigned char *b_s = smem + Layout::b;
-  unsigned char *ring = smem + Layout::ring;
+  unsigned char *ring = smem + layout_ring(p.fn_terms);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.m + UT - 1) / UT;
@@ -337,7 +387,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int u_begin = int((long long)blockIdx.x * units / gridDim.x);
   const int u_end = int((long long)(blockIdx.x + 1) * units / gridDim.x);
   const int n_units = u_end - u_begin;             // >= 1: the grid is at most `units`
-  const int nslot = ring_slots(p.tp), sbytes = slot_bytes(p.tp);
+  const int nslot = ring_slots(p.tp, p.fn_terms), sbytes = slot_bytes(p.tp);
   const int total_fills = n_units * NSTAGE;
   const int first_group = u_begin / n_tiles;
 
@@ -373,24 +423,29 @@ __global__ void __launch_bounds__(NT, 1)
       tc::mbar_init(bfull, 1);
       *abort_s = 0;
       tc::mbar_init_fence();
-      // the first group's hc_fn rows before anything else
-      stage_hc_fn(p, first_group, a_s, bfull);
       tc::tma_prefetch_desc(&tm_part);
       tc::tma_prefetch_desc(&tm_res);
       tc::tma_prefetch_desc(&tm_post);
       tc::tma_prefetch_desc(&tm_comb);
     }
     __syncwarp();
+    // the first group's weight rows before anything else
+    stage_hc_fn(p, first_group, a_s, bfull);
     for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
-    // the later groups' hc_fn rows, so that their staging copies read L2
+    // the later groups' weight rows, so that their staging copies read L2
     const int last_group = (u_end - 1) / n_tiles;
     for (int g = first_group + 1; g <= last_group && g <= first_group + 16; ++g) {
-      const uint32_t bytes = uint32_t(group_rows(p.hidden, g) * MIX * 4);
-      for (int j = 0; j < HC; ++j) {
-        const float *src = p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX;
-        if (tc::elect_one()) tc::prefetch_l2(src, bytes);
-        __syncwarp();
+      const int rows = group_rows(p.hidden, g);
+      if (p.fn_terms == 3) {
+        for (int j = lane; j < HC; j += 32)
+          tc::prefetch_l2(p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX, uint32_t(rows * MIX * 4));
+      } else {
+        for (int n = lane; n < MIX * HC; n += 32)
+          tc::prefetch_l2(p.hc_fn_bf16 + (size_t)(n % MIX) * HC * p.hidden + (size_t)(n / MIX) * p.hidden +
+                              (size_t)g * UK,
+                          uint32_t(rows * 2));
       }
+      __syncwarp();
     }
   } else if (warp == MMA_WARP) {
     tc::tmem_alloc(slot, TMEM_COLS);
@@ -430,7 +485,7 @@ __global__ void __launch_bounds__(NT, 1)
       const uint32_t d = tmem + uint32_t(nm & 1) * D_STRIDE;
       if (tc::elect_one()) {
 #pragma unroll 1
-        for (int term = 0; term < 3; ++term) {
+        for (int term = 0; term < p.fn_terms; ++term) {
 #pragma unroll
           for (int ks = 0; ks < UK / 16; ++ks) {
             const uint64_t ad = a0 + uint64_t((2 * ks * A_KCOL) >> 4);
@@ -480,16 +535,13 @@ __global__ void __launch_bounds__(NT, 1)
         // B and the A space change (the previous unit's MMAs are done); the
         // first group's rows were staged at kernel start, so their split
         // overlaps the first unit's loads and post-mix
-        if (cur_group >= 0 && warp == 0) {
-          if (tc::elect_one()) stage_hc_fn(p, g, a_s, bfull);
-          __syncwarp();
-        }
+        if (cur_group >= 0 && warp == 0) stage_hc_fn(p, g, a_s, bfull);
         if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
           *abort_s = 1;
           break;
         }
         ++loads;
-        convert_b(reinterpret_cast<const float *>(a_s), group_rows(p.hidden, g), b_s);
+        build_b(p, g, a_s, b_s);
         // every mixer has read the staged rows before any A row is written
         asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
         cur_group = g;
@@ -560,6 +612,7 @@ cudaError_t stage_tc_set_attributes() {
 cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream) {
   if (p.tp < 1 || p.tp > TP_TMA_MAX) return cudaErrorInvalidValue;
   if (p.slices != (p.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS) return cudaErrorInvalidValue;
+  if (!(p.fn_terms == 3 && p.hc_fn) && !(p.fn_terms == 1 && p.hc_fn_bf16)) return cudaErrorInvalidValue;
   const cuuint64_t H = cuuint64_t(p.hidden), M = cuuint64_t(p.m), TP = cuuint64_t(p.tp);
   CUtensorMap tm_part, tm_res, tm_post, tm_comb;
   const cuuint64_t part_dims[3] = {H, M, TP}, part_strides[2] = {H * 2, M * H * 2};
@@ -577,7 +630,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
     return cudaErrorInvalidValue;
   const int units = ((p.m + UT - 1) / UT) * p.slices;
   const int grid = units < ctas ? units : ctas;
-  const size_t smem = size_t(Layout::ring) + size_t(ring_slots(p.tp)) * slot_bytes(p.tp);
+  const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
   k_stage_tc<<<grid, NT, smem, stream>>>(p, tm_part, tm_res, tm_post, tm_comb);
   return cudaGetLastError();
 }

@@ -40,7 +40,9 @@ struct StageParams {
   const uint16_t *residual;   // [m][4][H]
   const float *post;          // [m][4]
   const float *comb;          // [m][4][4]
-  const float *hc_fn;         // [4H][24]
+  const float *hc_fn;         // [4H][24] f32, or null
+  const uint16_t *hc_fn_bf16; // [24][4H] bf16 (tensor-core kernel only), or null
+  int fn_terms;               // BF16 terms of B: 3 for the FP32 weight, 1 for the BF16 one
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares

@@ -110,7 +110,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   struct Need { const void *p; const char *name; size_t align; };
   const Need required[] = {
       {a->partials, "partials", 16}, {a->residual, "residual", 16}, {a->post, "post", 16},
-      {a->comb, "comb", 16}, {a->hc_fn, "hc_fn", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
+      {a->comb, "comb", 16}, {a->scale, "scale", 4}, {a->base, "base", 4},
       {a->norm_weight, "norm_weight", 16}, {a->residual_out, "residual_out", 16},
       {a->layer_input, "layer_input", 16}, {a->post_out, "post_out", 4}, {a->comb_out, "comb_out", 4}};
   for (const Need &n : required) {
@@ -126,6 +126,12 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
       return report(error, error_len, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
   if ((a->mxfp8_values == nullptr) != (a->mxfp8_scales == nullptr))
     return report(error, error_len, MHC_ERR_INVALID_ARG, "mxfp8_values and mxfp8_scales go together");
+  if ((a->hc_fn == nullptr) == (a->hc_fn_bf16 == nullptr))
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "exactly one of hc_fn and hc_fn_bf16 is required");
+  if (!aligned(a->hc_fn ? static_cast<const void *>(a->hc_fn) : a->hc_fn_bf16, 16))
+    return report(error, error_len, MHC_ERR_INVALID_ARG, "the prenorm weight is not 16-byte aligned");
+  if (a->hc_fn_bf16 && c.tp > TP_TMA_MAX)
+    return report(error, error_len, MHC_ERR_UNSUPPORTED, "hc_fn_bf16 needs tp <= %d", TP_TMA_MAX);
   if (a->mxfp8_values && !(c.flags & MHC_FLAG_MXFP8))
     return report(error, error_len, MHC_ERR_UNSUPPORTED, "MXFP8 outputs need MHC_FLAG_MXFP8");
 
@@ -155,6 +161,8 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.post = a->post;
   sp.comb = a->comb;
   sp.hc_fn = a->hc_fn;
+  sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
+  sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;

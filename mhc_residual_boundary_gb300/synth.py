@@ -46,6 +46,7 @@ class Workload:
     top_k: int = 0
     moe: bool = False
     mxfp8: bool = False
+    bf16_fn: bool = False    # prenorm weight as BF16 [24][4H] instead of FP32 [4H][24]
 
 
 # The workloads this boundary is measured and checked on.
@@ -55,6 +56,8 @@ WORKLOADS = {
     "glm": [Workload("glm", 6144, 4, 1 << i) for i in range(10)],
     "moe": [Workload("moe", 5120, 8, 256, top_k=8, moe=True)],
     "large_mxfp8": [Workload("large_mxfp8", 6144, 8, 4096, mxfp8=True)],
+    # the GLM shapes with the weight in the GLM page's BF16 [24][4H] form
+    "glm_bf16fn": [Workload("glm_bf16fn", 6144, 4, m, bf16_fn=True) for m in (1, 64, 256, 512)],
 }
 
 
@@ -118,4 +121,7 @@ def bf16_weight(hc_fn: np.ndarray) -> np.ndarray:
 
 
 def inputs_for(w: Workload, seed: int = 0) -> dict:
-    return make_inputs(w.hidden, w.tp, w.m, top_k=w.top_k, moe=w.moe, seed=seed)
+    out = make_inputs(w.hidden, w.tp, w.m, top_k=w.top_k, moe=w.moe, seed=seed)
+    if w.bf16_fn:
+        out["hc_fn_bf16"] = bf16_weight(out.pop("hc_fn"))
+    return out

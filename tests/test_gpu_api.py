@@ -53,6 +53,8 @@ def _untouched(outs):
     ("null_partials", "MHC_ERR_INVALID_ARG"), ("misaligned_partials", "MHC_ERR_INVALID_ARG"),
     ("misaligned_layer_input", "MHC_ERR_INVALID_ARG"), ("mxfp8_without_flag", "MHC_ERR_UNSUPPORTED"),
     ("misaligned_post", "MHC_ERR_INVALID_ARG"),
+    ("both_weight_forms", "MHC_ERR_INVALID_ARG"), ("no_weight", "MHC_ERR_INVALID_ARG"),
+    ("misaligned_bf16_weight", "MHC_ERR_INVALID_ARG"),
 ])
 def test_bad_arguments_launch_nothing(env, case, status):
     b, inp, capi = env
@@ -76,6 +78,13 @@ def test_bad_arguments_launch_nothing(env, case, status):
     elif case == "mxfp8_without_flag":
         a.mxfp8_values = spare.data_ptr()
         a.mxfp8_scales = spare.data_ptr()
+    elif case == "both_weight_forms":
+        a.hc_fn_bf16 = spare.data_ptr()
+    elif case == "no_weight":
+        a.hc_fn = None
+    elif case == "misaligned_bf16_weight":
+        a.hc_fn = None
+        a.hc_fn_bf16 = spare.data_ptr() + 2
     with pytest.raises(capi.MhcError) as err:
         capi.mhc_boundary_run(b.handle, a)
     assert status in str(err.value)

@@ -22,8 +22,11 @@ def Boundary():
 
 
 def check(Boundary, hidden, tp, m, *, seed=0, moe=False, top_k=0, mxfp8=False, holes=0.0,
-          capacity=None, mutate=None, **cfg):
+          capacity=None, mutate=None, bf16_weight=False, **cfg):
     inp = synth.make_inputs(hidden, tp, m, top_k=top_k, moe=moe, seed=seed, holes=holes)
+    if bf16_weight:
+        # the GLM page's form of the weight, BF16 [24][4H], instead of hc_fn
+        inp["hc_fn_bf16"] = synth.bf16_weight(inp.pop("hc_fn"))
     if mutate:
         mutate(inp)
     p = oracle.Problem(hidden, tp, m, top_k=top_k, rows_per_rank=m * top_k if moe else 0, **cfg)
@@ -73,6 +76,18 @@ def test_large_mxfp8(Boundary):
                                          (16384, 8, 40)])
 def test_ragged_shapes(Boundary, hidden, tp, m):
     check(Boundary, hidden, tp, m, seed=hidden + m)
+
+
+@pytest.mark.parametrize("hidden,tp,m,mxfp8", [(6144, 4, 1, False), (6144, 4, 256, False), (5120, 8, 64, False),
+                                               (520, 5, 33, False), (1000, 8, 300, False), (8, 1, 3, False),
+                                               (2048, 4, 130, True)])
+def test_bf16_weight(Boundary, hidden, tp, m, mxfp8):
+    # the prenorm weight as BF16 [24][4H] ([GLM] fn): one BF16 term in the MMAs
+    check(Boundary, hidden, tp, m, mxfp8=mxfp8, bf16_weight=True, seed=7 * m + hidden)
+
+
+def test_bf16_weight_moe(Boundary):
+    check(Boundary, 1024, 4, 60, moe=True, top_k=4, holes=0.2, bf16_weight=True, seed=17)
 
 
 @pytest.mark.parametrize("m", [1, 127, 129, 300])
