@@ -75,7 +75,7 @@ class OracleIO(ctypes.Structure):
         "partials", "routed", "idx", "weights", "shared", "residual", "post",
         "comb", "hc_fn", "hc_fn_bf16", "scale", "base", "gamma", "residual_out",
         "layer_input", "post_out", "comb_out", "mixes", "pre", "reduced",
-        "mx_values", "mx_scales")]
+        "mx_values", "mx_scales", "pre_in")]
 
 
 def _load():
@@ -235,6 +235,25 @@ def prenorm_gemv(streams, hc_fn):
     return raw, ss
 
 
+def consume(problem: Problem, inputs: dict, pre, *, moe: bool = False, mxfp8_out: bool = False,
+            residual_only: bool = False) -> dict:
+    """[DSV] AllReduceMHC's delayed-mHC consumer: stage 1 (or the MoE fold),
+    the post-mix, and the collapse + RMSNorm with the carried pre-mix ``pre``
+    [m][4] (no GEMV, no mixes); with ``residual_only`` the post-mixed streams
+    alone."""
+    m, hidden = problem.m, problem.hidden
+    outputs = {"residual_out": np.zeros((m, HC, hidden), np.uint16),
+               "reduced": np.zeros((m, hidden), np.uint16)}
+    if not residual_only:
+        outputs["layer_input"] = np.zeros((m, hidden), np.uint16)
+        if mxfp8_out:
+            outputs["mx_values"] = np.zeros((m, hidden), np.uint8)
+            outputs["mx_scales"] = np.full((mxfp8_scale_bytes(m, hidden),), 0xAB, np.uint8)
+    ins = dict(inputs)
+    ins["pre_in"] = _arr(pre, np.float32, (m, HC))
+    return boundary(problem, ins, moe=moe, mxfp8_out=mxfp8_out and not residual_only, outputs=outputs)
+
+
 def prenorm_gemv_bf16(streams, fn):
     """The GEMV with the weight as BF16 [24][4H] (the GLM page's layout)."""
     m, _, hidden = streams.shape
@@ -339,7 +358,7 @@ def boundary(problem: Problem, inputs: dict, *, moe: bool = False,
     for name, dtype in (("partials", np.uint16), ("routed", np.uint16), ("idx", np.int32),
                         ("weights", np.float32), ("shared", np.uint16), ("residual", np.uint16),
                         ("post", np.float32), ("comb", np.float32), ("hc_fn", np.float32),
-                        ("hc_fn_bf16", np.uint16),
+                        ("hc_fn_bf16", np.uint16), ("pre_in", np.float32),
                         ("scale", np.float32), ("base", np.float32), ("gamma", np.uint16)):
         setattr(io, name, ptr(name, dtype, inputs))
     for name in ("residual_out", "layer_input", "post_out", "comb_out", "mixes", "pre",

@@ -399,7 +399,9 @@ int oracle_boundary(const oracle_config_t *c, int32_t t0, int32_t t1, int moe,
                     const oracle_io_t *io) {
   /* [GLM] AllReduceMhcBoundary.__call__ order: stage 1 (or the MoE fold),
    * post-mix, prenorm GEMV, mixes and pre, collapse + RMSNorm; then the side
-   * kernel's post and Sinkhorn; [DSV] adds the MXFP8 copy. */
+   * kernel's post and Sinkhorn; [DSV] adds the MXFP8 copy.  With io->pre_in
+   * set, [DSV] AllReduceMHC's delayed-mHC consumer instead: stage 1, post-mix,
+   * and the collapse with the carried pre (or the streams alone). */
   if (!c || c->hidden <= 0 || c->m <= 0 || t0 < 0 || t1 > c->m || t0 > t1) return -1;
   if (c->tp <= 0) return -1;
   if (moe) {
@@ -424,6 +426,15 @@ int oracle_boundary(const oracle_config_t *c, int32_t t0, int32_t t1, int moe,
     else
       oracle_stage1(c, t0, t1, io->partials, y);
     oracle_post_mix(c, t0, t1, y, io->residual, io->post, io->comb, io->residual_out);
+    if (io->pre_in) {
+      /* [DSV] AllReduceMHC.__call__ / finalize: the collapse takes the carried
+       * pre-mix; residual_only writes the post-mixed streams alone */
+      if (io->layer_input) {
+        oracle_collapse_norm(c, t0, t1, io->residual_out, io->pre_in, io->gamma, io->layer_input);
+        if (io->mx_values && io->mx_scales)
+          oracle_mxfp8(c, t0, t1, io->layer_input, io->mx_values, io->mx_scales, t1 == c->m);
+      }
+    } else {
     if (io->hc_fn_bf16)
       oracle_prenorm_gemv_bf16(c, t0, t1, io->residual_out, io->hc_fn_bf16, raw, ss);
     else
@@ -434,6 +445,7 @@ int oracle_boundary(const oracle_config_t *c, int32_t t0, int32_t t1, int moe,
     oracle_sinkhorn(c, t0, t1, mixes, io->scale, io->base, io->comb_out);
     if (io->mx_values && io->mx_scales)
       oracle_mxfp8(c, t0, t1, io->layer_input, io->mx_values, io->mx_scales, t1 == c->m);
+    }
   }
   if (!io->reduced) free(y);
   free(raw);

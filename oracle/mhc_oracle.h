@@ -129,6 +129,10 @@ typedef struct {
   uint16_t *reduced;
   uint8_t *mx_values;
   uint8_t *mx_scales;
+  /* [DSV] delayed-mHC consumer: when set, the carried pre-mix [m][4] of the
+   * collapse; there is no GEMV, no mixes, no post / Sinkhorn, and with
+   * layer_input NULL only the post-mixed streams are written (residual only). */
+  const float *pre_in;
 } oracle_io_t;
 
 int oracle_boundary(const oracle_config_t *c, int32_t t0, int32_t t1, int moe,
