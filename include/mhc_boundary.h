@@ -205,6 +205,49 @@ mhc_status_t mhc_boundary_run(mhc_boundary_t *b, const mhc_run_args_t *args,
 mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *args,
                                        mhc_stream_t stream);
 
+/* Arguments of a delayed-mHC consumer call ([DSV] AllReduceMHC.__call__ /
+ * finalize): the boundary without the prenorm GEMV, for a model that carries
+ * the pre-mix from elsewhere.
+ *   partials     [tp][m][H] bf16, or NULL to fold an unfinalised MoE output
+ *                (rows_per_rank, routed, idx, weights, shared as in
+ *                mhc_moe_args_t; needs top_k > 0)
+ *   residual, post, comb: as for mhc_boundary_run
+ *   pre          [m][4] f32: carried pre-mix of the collapse; NULL together
+ *                with norm_weight and layer_input for residual_only ([DSV]
+ *                AllReduceMHC(residual_only=True)): only the post-mixed
+ *                streams are written
+ *   norm_weight  [H] bf16
+ *   residual_out [m][4][H] bf16, layer_input [m][H] bf16 (NULL iff pre is NULL)
+ *   reduced_out  optional [m][H] bf16: the stage-1 sum
+ *   mxfp8_values / mxfp8_scales: optional, as for mhc_boundary_run, not with
+ *                residual_only ([DSV]: "a residual-only consumer has no layer
+ *                input to quantize")
+ * No post_out / comb_out / mixes: the consumer leaves the next mixes to the
+ * caller.  Runs the stage kernel without its GEMV and, unless residual_only,
+ * the finish kernel with the carried pre, both on `stream`. */
+typedef struct {
+  int32_t m;
+  const void *partials;
+  int32_t rows_per_rank;
+  const void *routed;
+  const int32_t *idx;
+  const float *weights;
+  const void *shared;
+  const void *residual;
+  const float *post;
+  const float *comb;
+  const float *pre;
+  const void *norm_weight;
+  void *residual_out;
+  void *layer_input;
+  void *reduced_out;
+  uint8_t *mxfp8_values;
+  uint8_t *mxfp8_scales;
+} mhc_consume_args_t;
+
+mhc_status_t mhc_boundary_consume(mhc_boundary_t *b, const mhc_consume_args_t *args,
+                                  mhc_stream_t stream);
+
 /* Makes `stream` wait for the last side-stream kernel ([GLM]
  * AllReduceMhcBoundary.join).  Cheap; may be called any number of times.
  * On a capturing stream it joins a side kernel of the same capture; a side

@@ -39,6 +39,7 @@ OUTPUT_SPECS = {
     "post_out": (torch.float32, lambda m, H: (m, HC)),
     "comb_out": (torch.float32, lambda m, H: (m, HC, HC)),
     "pre_out": (torch.float32, lambda m, H: (m, HC)),
+    "pre": (torch.float32, lambda m, H: (m, HC)),
     "mixes_out": (torch.float32, lambda m, H: (m, MIX)),
     "reduced_out": (torch.bfloat16, lambda m, H: (m, H)),
     "mxfp8_values": (torch.uint8, lambda m, H: (m, H)),
@@ -155,6 +156,38 @@ class Boundary:
         for n in ("routed", "idx", "weights", "shared"):
             setattr(args, n, inputs[n].data_ptr())
         capi.mhc_boundary_finalize_moe(self.handle, args, stream)
+        return outputs
+
+    def consume(self, inputs: dict, outputs: dict, stream=None) -> dict:
+        """The delayed-mHC consumer ([DSV] AllReduceMHC.__call__ / finalize):
+        inputs hold partials (or routed / idx / weights / shared), residual,
+        post, comb and, unless residual only, pre [m][4] and norm_weight;
+        outputs hold residual_out and, with pre, layer_input (optionally
+        reduced_out, mxfp8_values / mxfp8_scales)."""
+        m = outputs["residual_out"].shape[0]
+        a = capi.mhc_consume_args_t()
+        a.m = m
+        moe = inputs.get("partials") is None
+        K = self.top_k
+        rows = inputs["routed"].shape[1] if moe else 0
+        names = ["residual", "post", "comb"]
+        names += ["routed", "idx", "weights", "shared"] if moe else ["partials"]
+        if inputs.get("pre") is not None:
+            names += ["pre", "norm_weight"]
+        for n in names:
+            t = inputs[n]
+            dtype, shape = INPUT_SPECS[n] if n in INPUT_SPECS else OUTPUT_SPECS[n]
+            want = shape(self.tp, m, self.hidden, K, rows) if n in INPUT_SPECS else shape(m, self.hidden)
+            if t.dtype != dtype or tuple(t.shape) != want or not t.is_contiguous() or t.device.type != "cuda":
+                raise ValueError(f"{n}: expected contiguous cuda {dtype} {want}")
+            setattr(a, n, t.data_ptr())
+        a.rows_per_rank = rows
+        for n, t in outputs.items():
+            dtype, shape = OUTPUT_SPECS[n]
+            if t.dtype != dtype or tuple(t.shape) != shape(m, self.hidden) or not t.is_contiguous():
+                raise ValueError(f"{n}: expected contiguous {dtype} {shape(m, self.hidden)}")
+            setattr(a, n, t.data_ptr())
+        capi.mhc_boundary_consume(self.handle, a, stream)
         return outputs
 
     def run_host(self, inputs: dict, outputs: dict, stream=None) -> dict:

@@ -51,6 +51,13 @@ class mhc_moe_args_t(ctypes.Structure):
                 ("weights", ctypes.c_void_p), ("shared", ctypes.c_void_p)]
 
 
+class mhc_consume_args_t(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("partials", ctypes.c_void_p), ("rows_per_rank", ctypes.c_int32)] + [
+        (f, ctypes.c_void_p) for f in ("routed", "idx", "weights", "shared", "residual", "post", "comb", "pre",
+                                      "norm_weight", "residual_out", "layer_input", "reduced_out",
+                                      "mxfp8_values", "mxfp8_scales")]
+
+
 class mhc_profile_t(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_int32), ("stage_ms", ctypes.c_float), ("finish_ms", ctypes.c_float),
                 ("mixes_ms", ctypes.c_float)]
@@ -74,12 +81,14 @@ def lib() -> ctypes.CDLL:
         h.mhc_boundary_run_host.argtypes = [vp, ctypes.POINTER(mhc_run_args_t), vp]
         h.mhc_boundary_finalize_moe.argtypes = [vp, ctypes.POINTER(mhc_moe_args_t), vp]
         h.mhc_boundary_join.argtypes = [vp, vp]
+        h.mhc_boundary_consume.argtypes = [vp, ctypes.POINTER(mhc_consume_args_t), vp]
         h.mhc_boundary_check_errors.argtypes = [vp]
         h.mhc_boundary_destroy.argtypes = [vp]
         h.mhc_boundary_profile_begin.argtypes = [vp, ctypes.c_int32]
         h.mhc_boundary_profile_end.argtypes = [vp, ctypes.POINTER(mhc_profile_t)]
         for name in ("mhc_boundary_create", "mhc_boundary_run", "mhc_boundary_run_host",
-                     "mhc_boundary_finalize_moe", "mhc_boundary_join", "mhc_boundary_check_errors",
+                     "mhc_boundary_finalize_moe", "mhc_boundary_consume", "mhc_boundary_join",
+                     "mhc_boundary_check_errors",
                      "mhc_boundary_destroy", "mhc_boundary_profile_begin", "mhc_boundary_profile_end"):
             getattr(h, name).restype = st
         h.mhc_boundary_run_static.argtypes = [ctypes.POINTER(mhc_boundary_config_t),
@@ -128,6 +137,10 @@ def mhc_boundary_run_host(handle, args: mhc_run_args_t, stream=None) -> None:
 
 def mhc_boundary_finalize_moe(handle, args: mhc_moe_args_t, stream=None) -> None:
     _check(lib().mhc_boundary_finalize_moe(handle, ctypes.byref(args), _stream_ptr(stream)), handle)
+
+
+def mhc_boundary_consume(handle, args: mhc_consume_args_t, stream=None) -> None:
+    _check(lib().mhc_boundary_consume(handle, ctypes.byref(args), _stream_ptr(stream)), handle)
 
 
 def mhc_boundary_join(handle, stream=None) -> None:

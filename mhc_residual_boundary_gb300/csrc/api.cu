@@ -141,6 +141,55 @@ mhc_status_t validate_moe(const mhc_boundary *b, const mhc_moe_args_t *a, std::s
   return MHC_OK;
 }
 
+// Checks of one delayed-mHC consumer call.
+mhc_status_t validate_consume(const mhc_boundary *b, const mhc_consume_args_t *a, std::string &msg) {
+  const mhc_boundary_config_t &c = b->cfg;
+  if (!a) return fail(msg, MHC_ERR_INVALID_ARG, "args is NULL");
+  if (a->m < 1 || a->m > c.max_num_tokens)
+    return fail(msg, MHC_ERR_CAPACITY, "M=%d is outside [1, %d]", a->m, c.max_num_tokens);
+  struct Need { const void *p; const char *name; size_t align; };
+  const Need required[] = {{a->residual, "residual", 16}, {a->post, "post", 16}, {a->comb, "comb", 16},
+                           {a->residual_out, "residual_out", 16}};
+  for (const Need &n : required) {
+    if (!n.p) return fail(msg, MHC_ERR_INVALID_ARG, "%s is NULL", n.name);
+    if (!aligned(n.p, n.align))
+      return fail(msg, MHC_ERR_INVALID_ARG, "%s is not %zu-byte aligned", n.name, n.align);
+  }
+  if (a->partials) {
+    if (!aligned(a->partials, 16)) return fail(msg, MHC_ERR_INVALID_ARG, "partials is not 16-byte aligned");
+    if (c.tp > TP_TMA_MAX) return fail(msg, MHC_ERR_UNSUPPORTED, "the consumer needs tp <= %d", TP_TMA_MAX);
+  } else {
+    if (c.top_k < 1) return fail(msg, MHC_ERR_UNSUPPORTED, "no partials and created with top_k = 0");
+    if (a->rows_per_rank < 1) return fail(msg, MHC_ERR_INVALID_ARG, "rows_per_rank must be >= 1");
+    if (!a->routed || !a->idx || !a->weights || !a->shared)
+      return fail(msg, MHC_ERR_INVALID_ARG, "the MoE fold needs routed, idx, weights and shared");
+    if (!aligned(a->routed, 16) || !aligned(a->shared, 16))
+      return fail(msg, MHC_ERR_INVALID_ARG, "routed and shared must be 16-byte aligned");
+    if (!aligned(a->idx, 4) || !aligned(a->weights, 4))
+      return fail(msg, MHC_ERR_INVALID_ARG, "idx and weights must be 4-byte aligned");
+  }
+  if (a->reduced_out && !aligned(a->reduced_out, 16))
+    return fail(msg, MHC_ERR_INVALID_ARG, "reduced_out is not 16-byte aligned");
+  if ((a->mxfp8_values == nullptr) != (a->mxfp8_scales == nullptr))
+    return fail(msg, MHC_ERR_INVALID_ARG, "mxfp8_values and mxfp8_scales are both given or both NULL");
+  if (!a->pre) {
+    if (a->norm_weight || a->layer_input)
+      return fail(msg, MHC_ERR_INVALID_ARG, "residual only (pre NULL) takes no norm_weight or layer_input");
+    if (a->mxfp8_values)
+      return fail(msg, MHC_ERR_INVALID_ARG, "a residual-only consumer has no layer input to quantize");
+  } else {
+    if (!a->norm_weight || !a->layer_input)
+      return fail(msg, MHC_ERR_INVALID_ARG, "a carried pre needs norm_weight and layer_input");
+    if (!aligned(a->pre, 4) || !aligned(a->norm_weight, 16) || !aligned(a->layer_input, 16))
+      return fail(msg, MHC_ERR_INVALID_ARG, "pre, norm_weight or layer_input is misaligned");
+    if (a->mxfp8_values && !(c.flags & MHC_FLAG_MXFP8))
+      return fail(msg, MHC_ERR_UNSUPPORTED, "created without MHC_FLAG_MXFP8");
+    if (a->mxfp8_values && (!aligned(a->mxfp8_values, 16) || !aligned(a->mxfp8_scales, 16)))
+      return fail(msg, MHC_ERR_INVALID_ARG, "mxfp8 buffers must be 16-byte aligned");
+  }
+  return MHC_OK;
+}
+
 // The id of the capture `stream` is recording into, 0 when it is not capturing.
 cudaError_t capture_id(cudaStream_t stream, unsigned long long *id) {
   cudaStreamCaptureStatus status = cudaStreamCaptureStatusNone;
@@ -281,6 +330,71 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   if (on_side) {
     b->side_pending = true;
     b->side_capture = capture;
+  }
+  b->last_error.clear();
+  return MHC_OK;
+}
+
+// One delayed-mHC consumer call: the optional MoE fold, the stage kernel
+// without its GEMV, and (unless residual only) the finish kernel with the
+// carried pre-mix, all on `stream`.
+mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStream_t stream) {
+  const mhc_boundary_config_t &c = b->cfg;
+  unsigned long long capture = 0;
+  cudaError_t e = capture_id(stream, &capture);
+  if (e == cudaSuccess && side_join_needed(b, capture)) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+  StageParams sp = {};
+  sp.m = a->m;
+  sp.hidden = c.hidden;
+  sp.tp = c.tp;
+  sp.partials = static_cast<const uint16_t *>(a->partials);
+  if (!a->partials) {
+    FoldParams fo = {};
+    fo.m = a->m;
+    fo.hidden = c.hidden;
+    fo.tp = c.tp;
+    fo.top_k = c.top_k;
+    fo.rows_per_rank = a->rows_per_rank;
+    fo.routed = static_cast<const uint16_t *>(a->routed);
+    fo.idx = a->idx;
+    fo.weights = a->weights;
+    fo.shared = static_cast<const uint16_t *>(a->shared);
+    fo.y = b->fold;
+    fo.err = b->err;
+    e = launch_moe_fold(fo, b->sm_count * 16, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
+    sp.tp = 1;
+    sp.partials = b->fold;
+  }
+  sp.slices = (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS;
+  sp.residual = static_cast<const uint16_t *>(a->residual);
+  sp.post = a->post;
+  sp.comb = a->comb;
+  sp.fn_terms = 0;   // no GEMV
+  sp.residual_out = static_cast<uint16_t *>(a->residual_out);
+  sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+  sp.part = b->part;
+  sp.part_stride = part_row_floats(sp.slices);
+  sp.err = b->err;
+  e = launch_stage_tc(sp, b->sm_count, stream);
+  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
+  if (a->pre) {
+    FinishParams fp = {};
+    fp.m = a->m;
+    fp.hidden = c.hidden;
+    fp.slices = 0;
+    fp.part_stride = 0;
+    fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
+    fp.streams = static_cast<const uint16_t *>(a->residual_out);
+    fp.norm_eps = c.norm_eps;
+    fp.pre_in = a->pre;
+    fp.layer_input = static_cast<uint16_t *>(a->layer_input);
+    fp.mx_values = a->mxfp8_values;
+    fp.mx_scales = a->mxfp8_scales;
+    fp.err = b->err;
+    e = launch_finish(fp, b->sm_count, stream, true);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
   }
   b->last_error.clear();
   return MHC_OK;
@@ -433,6 +547,18 @@ mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *
   }
   DeviceGuard guard(b->device);
   return launch_call(b, &args->run, args, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mhc_status_t mhc_boundary_consume(mhc_boundary_t *b, const mhc_consume_args_t *args, mhc_stream_t stream) {
+  if (!b) return MHC_ERR_INVALID_ARG;
+  std::string msg;
+  const mhc_status_t s = validate_consume(b, args, msg);
+  if (s != MHC_OK) {
+    b->last_error = msg;
+    return s;
+  }
+  DeviceGuard guard(b->device);
+  return consume_call(b, args, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream) {

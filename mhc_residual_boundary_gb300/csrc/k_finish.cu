@@ -14,6 +14,8 @@
 //     out * 2^(127 - e) with hardware nearest-even satfinite conversions,
 //     scales at the 128x4 swizzled offset, padding-row scales zeroed ([DSV]
 //     _LamportMHCDeviceKernel.kernel, quantize branch);
+//  With `pre_in` set (the [DSV] delayed-mHC consumer) steps 1-2 and 5 are
+//  skipped: the collapse takes the carried pre-mix.
 //  5. with `post_out` set, the next boundary's post-mix and Sinkhorn residual
 //     mix as well ([GLM] _MixesDeviceKernel.kernel and _sinkhorn): the mixes
 //     warp keeps the normalised mixes of up to 32 of the CTA's tokens and
@@ -185,7 +187,8 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   const int H = p.hidden;
   const int nfrag = H / VEC;
   const size_t sbytes = slot_bytes(H, p.part_stride);
-  const uint32_t stream_bytes = uint32_t(HC) * H * 2, part_bytes = uint32_t(p.part_stride) * 4;
+  const uint32_t stream_bytes = uint32_t(HC) * H * 2;
+  const uint32_t part_bytes = p.pre_in ? 0u : uint32_t(p.part_stride) * 4;   // no GEMV sums with a carried pre
   // tokens of this CTA: blockIdx.x + k * gridDim.x, k < n_tok
   const int n_tok = (p.m - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
 
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
     uint64_t *bar = &full[k % slots];
     tc::mbar_arrive_expect_tx(bar, stream_bytes + part_bytes);
     tc::bulk_load_hint(dst, p.streams + (size_t)t * HC * H, stream_bytes, bar, read_once);
-    tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, bar);
+    if (part_bytes) tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, bar);
   };
   int filled = 0;   // tokens whose copies were issued (thread 0)
   if (tid == 0)
@@ -221,7 +224,10 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
 
     // 1.-2. (mixes warp) each of lanes 0-24 sums one value over the groups
     // in group order; rstd, the mixes, pre (shared with the collapse warps)
-    if (warp == MIX_WARP) {
+    if (warp == MIX_WARP && p.pre_in) {
+      // the delayed-mHC consumer: the collapse takes the carried pre-mix
+      if (lane < HC) pre_s[lane] = p.pre_in[(size_t)t * HC + lane];
+    } else if (warp == MIX_WARP) {
       float v = 0.f;
       if (lane < VALUES)
         for (int g = 0; g < p.slices; ++g) v = __fadd_rn(v, part_s[g * VALUES + lane]);
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
       // (fused) post + Sinkhorn per batch of tokens, one token per lane,
       // beside the batch's last collapse
       const int b = k % BATCH;
-      if (p.post_out && (b == BATCH - 1 || k == n_tok - 1)) {
+      if (p.post_out && !p.pre_in && (b == BATCH - 1 || k == n_tok - 1)) {
         const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
         if (lane <= b) post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
         __syncwarp();

@@ -112,8 +112,9 @@ struct Layout {
 };
 __host__ __device__ constexpr int layout_a(int terms) { return Layout::b + terms * TERM_BYTES; }
 __host__ __device__ constexpr int layout_ring(int terms) {
-  return layout_a(terms) + (terms == 3 ? (A_BYTES > STAGING ? A_BYTES : STAGING)
-                                       : (A_BYTES > STAGING_BF16 ? A_BYTES : STAGING_BF16));
+  return terms == 0 ? Layout::b   // no GEMV (the delayed-mHC consumer): neither B nor A
+                    : layout_a(terms) + (terms == 3 ? (A_BYTES > STAGING ? A_BYTES : STAGING)
+                                                    : (A_BYTES > STAGING_BF16 ? A_BYTES : STAGING_BF16));
 }
 static_assert(layout_ring(3) % 128 == 0 && layout_ring(1) % 128 == 0, "TMA alignment");
 
@@ -216,28 +217,24 @@ __device__ __forceinline__ int group_rows(int hidden, int g) {
 
 // Group g's weight rows into `stg`, counted on `bar`; called by a whole warp.
 // FP32 weight: four bulk copies (one per stream, 128 rows of 24 floats).
-// BF16 weight: 96 bulk copies of 256-byte row pieces, three per lane.
-__device__ __forceinline__ void stage_hc_fn(const StageParams &p, int g, unsigned char *stg, uint64_t *bar) {
+// BF16 weight: four tiled copies (one per stream: 24 rows of 128 columns).
+__device__ __forceinline__ void stage_hc_fn(const StageParams &p, const CUtensorMap *tm_fn, int g,
+                                            unsigned char *stg, uint64_t *bar) {
   const int rows = group_rows(p.hidden, g);
-  if (p.fn_terms == 3) {
-    if (tc::elect_one()) {
+  if (tc::elect_one()) {
+    if (p.fn_terms == 3) {
       tc::mbar_arrive_expect_tx(bar, uint32_t(HC * rows * MIX * 4));
       for (int j = 0; j < HC; ++j)
         tc::bulk_load(stg + j * HC_ROWS_BYTES, p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX,
                       uint32_t(rows * MIX * 4), bar);
+    } else {
+      // the full boxes arrive (columns past the weight are zero-filled)
+      tc::mbar_arrive_expect_tx(bar, uint32_t(HC * MIX * FN_SEG));
+      for (int j = 0; j < HC; ++j)
+        tc::tma_load_2d(stg + j * MIX * FN_SEG, tm_fn, j * p.hidden + g * UK, 0, bar);
     }
-    __syncwarp();
-  } else {
-    if (tc::elect_one()) tc::mbar_arrive_expect_tx(bar, uint32_t(MIX * HC * rows * 2));
-    __syncwarp();
-    for (int n = threadIdx.x & 31; n < MIX * HC; n += 32) {
-      const int j = n / MIX, i = n % MIX;
-      tc::bulk_load(stg + n * FN_SEG,
-                    p.hc_fn_bf16 + (size_t)i * HC * p.hidden + (size_t)j * p.hidden + (size_t)g * UK,
-                    uint32_t(rows * 2), bar);
-    }
-    __syncwarp();
   }
+  __syncwarp();
 }
 
 // Splits (FP32) or places (BF16) the staged weight rows of group g into B.
@@ -368,7 +365,7 @@ __device__ __forceinline__ float mix_item(Item &it, uint4 &yb, uint4 (&nv)[HC]) 
 __global__ void __launch_bounds__(NT, 1)
     k_stage_tc(const StageParams p, const __grid_constant__ CUtensorMap tm_part,
                const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_post,
-               const __grid_constant__ CUtensorMap tm_comb) {
+               const __grid_constant__ CUtensorMap tm_comb, const __grid_constant__ CUtensorMap tm_fn) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Layout::full);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Layout::empty);
@@ -390,6 +387,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int nslot = ring_slots(p.tp, p.fn_terms), sbytes = slot_bytes(p.tp);
   const int total_fills = n_units * NSTAGE;
   const int first_group = u_begin / n_tiles;
+  const bool gemv = p.fn_terms > 0;                // false: streams only (delayed-mHC consumer)
 
   // The finish kernel may be scheduled on SMs as they free up; it waits for
   // this whole grid (and its memory) before it reads anything this grid writes.
@@ -427,23 +425,21 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tma_prefetch_desc(&tm_res);
       tc::tma_prefetch_desc(&tm_post);
       tc::tma_prefetch_desc(&tm_comb);
+      if (p.fn_terms == 1) tc::tma_prefetch_desc(&tm_fn);
     }
     __syncwarp();
     // the first group's weight rows before anything else
-    stage_hc_fn(p, first_group, a_s, bfull);
+    if (gemv) stage_hc_fn(p, &tm_fn, first_group, a_s, bfull);
     for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
     // the later groups' weight rows, so that their staging copies read L2
-    const int last_group = (u_end - 1) / n_tiles;
+    const int last_group = gemv ? (u_end - 1) / n_tiles : first_group;
     for (int g = first_group + 1; g <= last_group && g <= first_group + 16; ++g) {
       const int rows = group_rows(p.hidden, g);
       if (p.fn_terms == 3) {
         for (int j = lane; j < HC; j += 32)
           tc::prefetch_l2(p.hc_fn + ((size_t)j * p.hidden + (size_t)g * UK) * MIX, uint32_t(rows * MIX * 4));
       } else {
-        for (int n = lane; n < MIX * HC; n += 32)
-          tc::prefetch_l2(p.hc_fn_bf16 + (size_t)(n % MIX) * HC * p.hidden + (size_t)(n / MIX) * p.hidden +
-                              (size_t)g * UK,
-                          uint32_t(rows * 2));
+        for (int j = lane; j < HC; j += 32) tc::tma_prefetch_2d(&tm_fn, j * p.hidden + g * UK, 0);
       }
       __syncwarp();
     }
@@ -476,7 +472,7 @@ __global__ void __launch_bounds__(NT, 1)
     const uint64_t a0 = tc::smem_desc(tc::smem_addr(a_s), A_KCOL, 128);
     const uint64_t b0 = tc::smem_desc(tc::smem_addr(b_s), B_KCOL, 128);
     int nm = 0;
-    for (; nm < n_units; ++nm) {
+    for (; gemv && nm < n_units; ++nm) {
       if (!tc::mbar_wait_bounded(afull, uint32_t(nm & 1), WAIT_LIMIT) || *abort_s) {
         if (lane == 0) *abort_s = 1;
         break;
@@ -528,6 +524,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
         for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
       }
+      if (!gemv) continue;
       // the A buffer is free once the previous unit's MMAs are done
       if (ep.i >= 0) epilogue(ep);
       ep.i = -1;
@@ -535,7 +532,7 @@ __global__ void __launch_bounds__(NT, 1)
         // B and the A space change (the previous unit's MMAs are done); the
         // first group's rows were staged at kernel start, so their split
         // overlaps the first unit's loads and post-mix
-        if (cur_group >= 0 && warp == 0) stage_hc_fn(p, g, a_s, bfull);
+        if (cur_group >= 0 && warp == 0) stage_hc_fn(p, &tm_fn, g, a_s, bfull);
         if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
           *abort_s = 1;
           break;
@@ -612,9 +609,10 @@ cudaError_t stage_tc_set_attributes() {
 cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream) {
   if (p.tp < 1 || p.tp > TP_TMA_MAX) return cudaErrorInvalidValue;
   if (p.slices != (p.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS) return cudaErrorInvalidValue;
-  if (!(p.fn_terms == 3 && p.hc_fn) && !(p.fn_terms == 1 && p.hc_fn_bf16)) return cudaErrorInvalidValue;
+  if (!(p.fn_terms == 3 && p.hc_fn) && !(p.fn_terms == 1 && p.hc_fn_bf16) && p.fn_terms != 0)
+    return cudaErrorInvalidValue;
   const cuuint64_t H = cuuint64_t(p.hidden), M = cuuint64_t(p.m), TP = cuuint64_t(p.tp);
-  CUtensorMap tm_part, tm_res, tm_post, tm_comb;
+  CUtensorMap tm_part, tm_res, tm_post, tm_comb, tm_fn = {};
   const cuuint64_t part_dims[3] = {H, M, TP}, part_strides[2] = {H * 2, M * H * 2};
   const cuuint32_t part_box[3] = {UK, QT, cuuint32_t(p.tp)};
   const cuuint64_t res_dims[3] = {H, HC, M}, res_strides[2] = {H * 2, HC * H * 2};
@@ -628,10 +626,17 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
       !encode(&tm_post, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.post, post_dims, post_strides, post_box) ||
       !encode(&tm_comb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.comb, comb_dims, comb_strides, comb_box))
     return cudaErrorInvalidValue;
+  if (p.fn_terms == 1) {
+    // the BF16 weight [24][4H]: box of 128 columns x 24 rows (one stream of a group)
+    const cuuint64_t fn_dims[2] = {HC * H, MIX}, fn_strides[1] = {HC * H * 2};
+    const cuuint32_t fn_box[2] = {UK, MIX};
+    if (!encode(&tm_fn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.hc_fn_bf16, fn_dims, fn_strides, fn_box))
+      return cudaErrorInvalidValue;
+  }
   const int units = ((p.m + UT - 1) / UT) * p.slices;
   const int grid = units < ctas ? units : ctas;
   const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
-  k_stage_tc<<<grid, NT, smem, stream>>>(p, tm_part, tm_res, tm_post, tm_comb);
+  k_stage_tc<<<grid, NT, smem, stream>>>(p, tm_part, tm_res, tm_post, tm_comb, tm_fn);
   return cudaGetLastError();
 }
 

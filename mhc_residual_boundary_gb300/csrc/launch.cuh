@@ -42,7 +42,8 @@ struct StageParams {
   const float *comb;          // [m][4][4]
   const float *hc_fn;         // [4H][24] f32, or null
   const uint16_t *hc_fn_bf16; // [24][4H] bf16 (tensor-core kernel only), or null
-  int fn_terms;               // BF16 terms of B: 3 for the FP32 weight, 1 for the BF16 one
+  int fn_terms;               // BF16 terms of B: 3 for the FP32 weight, 1 for the BF16 one,
+                              // 0 for no GEMV (the delayed-mHC consumer: streams only)
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares
@@ -64,6 +65,7 @@ struct FinishParams {
   float rms_eps, hc_eps, norm_eps;
   float *mixes;               // [m][24] raw mixes for the side kernel, or null
   float *mixes_out;           // optional copy
+  const float *pre_in;        // [m][4] carried pre-mix (delayed-mHC consumer), or null
   float *post_out;            // [m][4]: post-mix computed here (fused), or null
   float *comb_out;            // [m][4][4]: Sinkhorn mix computed here (fused), or null
   float post_mult;

@@ -98,6 +98,12 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
       ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
       : "memory");
 }
+// Prefetches a tiled box into L2 without waiting.
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1)
+               : "memory");
+}
 // Contiguous bulk copy global -> shared memory (both addresses 16-byte
 // aligned, bytes a multiple of 16), counted on the mbarrier.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

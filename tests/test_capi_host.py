@@ -46,6 +46,7 @@ def test_struct_layouts_match_the_header(capi, tmp_path):
         "mhc_boundary_config_t": capi.mhc_boundary_config_t,
         "mhc_run_args_t": capi.mhc_run_args_t,
         "mhc_moe_args_t": capi.mhc_moe_args_t,
+        "mhc_consume_args_t": capi.mhc_consume_args_t,
         "mhc_profile_t": capi.mhc_profile_t,
     }
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "mhc_boundary.h"', "int main(void) {"]
