@@ -62,7 +62,8 @@ def workload(name, m):
     w = cands[-1] if m is None else next((c for c in cands if c.m == m), None)
     if w is None:
         base = cands[-1]
-        w = synth.Workload(base.name, base.hidden, base.tp, m, base.top_k, base.moe, base.mxfp8, base.bf16_fn)
+        w = synth.Workload(base.name, base.hidden, base.tp, m, base.top_k, base.moe, base.mxfp8, base.bf16_fn,
+                           base.consume, base.residual_only)
     return w
 
 
@@ -74,6 +75,11 @@ def call_bytes(w):
         stage1 = tp * K * 2 * H + tp * 2 * H + tp * K * 4 + K * 4
     else:
         stage1 = 2 * tp * H
+    if w.consume:
+        # the delayed-mHC consumer: no weight, no mixes; pre read, layer input written
+        stage = M * (stage1 + 8 * H + 8 * H + 16 + 64)
+        finish = 0 if w.residual_only else 2 * H + M * (16 + 2 * H)
+        return {"stage": stage, "finish": finish, "mixes": 0, "total": stage + finish}
     stage = M * (stage1 + 8 * H + 8 * H + 16 + 64) + 4 * H * 24 * (2 if w.bf16_fn else 4)
     finish = 2 * H + M * 2 * H
     if w.mxfp8:
@@ -86,7 +92,8 @@ def call_bytes(w):
 def describe(w):
     return {"workload": w.name, "tokens": w.m, "hidden": w.hidden, "tp": w.tp, "hc": 4,
             "top_k": w.top_k, "moe": w.moe, "mxfp8": w.mxfp8,
-            "weight": "bf16 [24][4H]" if w.bf16_fn else "f32 [4H][24]"}
+            "weight": "none (carried pre)" if w.consume else "bf16 [24][4H]" if w.bf16_fn else "f32 [4H][24]",
+            "residual_only": w.residual_only}
 
 
 # ------------------------------------------------------------------ ranks
@@ -406,9 +413,17 @@ def run_sweep(args):
             b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8)
             nbytes = call_bytes(w)
             nsets = 1 if nbytes["total"] >= 3 * l2 else math.ceil(3 * l2 / nbytes["total"]) + 1
-            sets = [(dev_in if s == 0 else {k: v.clone() for k, v in dev_in.items()},
-                     b.empty_outputs(w.m, mxfp8=w.mxfp8)) for s in range(nsets)]
-            call = b.finalize_moe if w.moe else b.run
+            def outputs():
+                o = b.empty_outputs(w.m, mxfp8=w.mxfp8)
+                if w.consume:
+                    o = {k: v for k, v in o.items()
+                         if k == "residual_out" or (k == "layer_input" and not w.residual_only)}
+                return o
+            if w.residual_only:
+                dev_in.pop("norm_weight", None)
+            sets = [(dev_in if s == 0 else {k: v.clone() for k, v in dev_in.items()}, outputs())
+                    for s in range(nsets)]
+            call = b.consume if w.consume else b.finalize_moe if w.moe else b.run
             steps = max(args.steps, nsets)
             for i in range(max(args.warmup, 3)):
                 call(*sets[i % nsets], stream=stream)

@@ -124,13 +124,19 @@ __host__ __device__ constexpr int slot_res(int tp) { return tp * QT * ROW; }
 __host__ __device__ constexpr int slot_post(int tp) { return slot_res(tp) + QT * HC * ROW; }
 __host__ __device__ constexpr int slot_comb(int tp) { return slot_post(tp) + QT * HC * 4; }
 __host__ __device__ constexpr int slot_bytes(int tp) { return slot_comb(tp) + QT * HC * HC * 4; }
+// Ring slots: a multiple of the four stages of a unit, so that slot
+// n % nslot always serves stage n % 4 and every use of a slot is consumed by
+// the same four warps in order.  (With, say, six slots a slot would alternate
+// between two stages' warps, and a warp waiting for the slot's use two ahead
+// could pass on the parity of the use before it.)
 __host__ __device__ constexpr int ring_slots(int tp, int terms) {
-  return (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) < MAX_SLOTS
-             ? (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp)
-             : MAX_SLOTS;
+  return ((SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) < MAX_SLOTS
+              ? (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp)
+              : MAX_SLOTS) / NSTAGE * NSTAGE;
 }
 static_assert(slot_bytes(1) % 128 == 0 && slot_post(1) % 128 == 0 && slot_comb(1) % 128 == 0, "slot alignment");
 static_assert(ring_slots(TP_TMA_MAX, 3) >= NSTAGE, "a unit's four stages fit the ring");
+static_assert(MAX_SLOTS % NSTAGE == 0, "slot n % nslot serves stage n % 4");
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 __device__ __forceinline__ float lane4(const float4 &v, int j) {

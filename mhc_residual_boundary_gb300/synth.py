@@ -47,6 +47,8 @@ class Workload:
     moe: bool = False
     mxfp8: bool = False
     bf16_fn: bool = False    # prenorm weight as BF16 [24][4H] instead of FP32 [4H][24]
+    consume: bool = False    # the delayed-mHC consumer: carried pre, no GEMV
+    residual_only: bool = False
 
 
 # The workloads this boundary is measured and checked on.
@@ -58,6 +60,10 @@ WORKLOADS = {
     "large_mxfp8": [Workload("large_mxfp8", 6144, 8, 4096, mxfp8=True)],
     # the GLM shapes with the weight in the GLM page's BF16 [24][4H] form
     "glm_bf16fn": [Workload("glm_bf16fn", 6144, 4, m, bf16_fn=True) for m in (1, 64, 256, 512)],
+    "large_bf16fn": [Workload("large_bf16fn", 6144, 8, 4096, mxfp8=True, bf16_fn=True)],
+    # the delayed-mHC consumer (carried pre) and its residual-only form
+    "consume": [Workload("consume", 6144, 8, m, consume=True) for m in (1, 256, 4096)],
+    "residual_only": [Workload("residual_only", 6144, 8, 4096, consume=True, residual_only=True)],
 }
 
 
@@ -124,4 +130,7 @@ def inputs_for(w: Workload, seed: int = 0) -> dict:
     out = make_inputs(w.hidden, w.tp, w.m, top_k=w.top_k, moe=w.moe, seed=seed)
     if w.bf16_fn:
         out["hc_fn_bf16"] = bf16_weight(out.pop("hc_fn"))
+    if w.consume and not w.residual_only:
+        # a carried pre-mix: sigmoid outputs plus hc_eps lie in (0, 1]
+        out["pre"] = np.random.default_rng(seed + 7919).uniform(0.05, 1.0, (w.m, HC)).astype(np.float32)
     return out

@@ -86,6 +86,14 @@ def test_bf16_weight(Boundary, hidden, tp, m, mxfp8):
     check(Boundary, hidden, tp, m, mxfp8=mxfp8, bf16_weight=True, seed=7 * m + hidden)
 
 
+@pytest.mark.parametrize("hidden,tp,m,bf16", [(2048, 6, 1024, False), (2048, 3, 1024, False),
+                                              (6144, 8, 512, True), (2048, 8, 1024, True)])
+def test_ring_wraps_many_times(Boundary, hidden, tp, m, bf16):
+    # several units per CTA, so every ring slot is reused many times, at tp
+    # values whose slot count is not a multiple of a unit's four stages
+    check(Boundary, hidden, tp, m, bf16_weight=bf16, seed=hidden + tp + m)
+
+
 def test_bf16_weight_moe(Boundary):
     check(Boundary, 1024, 4, 60, moe=True, top_k=4, holes=0.2, bf16_weight=True, seed=17)
 
