@@ -178,11 +178,13 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
 template <int NF>
 __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[MAX_SLOTS];
-  __shared__ float pre_s[HC];
+  __shared__ __align__(8) uint64_t sfull[MAX_SLOTS];   // a slot's four stream rows arrived
+  __shared__ __align__(8) uint64_t pfull[MAX_SLOTS];   // a slot's partial-sum row arrived
+  __shared__ float pre_s[2][HC];                       // pre of token k in pre_s[k & 1]
   __shared__ float red_s[CWARPS];
   __shared__ float mix_s[BATCH][MIX];
-  __shared__ int abort_s;
+  __shared__ int abort_s;   // some wait gave up (reported after the loop)
+  bool bad = false;         // one of this thread's waits gave up
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = p.hidden;
   const int nfrag = H / VEC;
@@ -193,7 +195,10 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   const int n_tok = (p.m - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);
 
   if (tid == 0) {
-    for (int i = 0; i < slots; ++i) tc::mbar_init(&full[i], 1);
+    for (int i = 0; i < slots; ++i) {
+      tc::mbar_init(&sfull[i], 1);
+      tc::mbar_init(&pfull[i], 1);
+    }
     abort_s = 0;
     tc::mbar_init_fence();
   }
@@ -203,65 +208,84 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   pdl_wait();
 
   const uint64_t read_once = tc::policy_evict_first();   // the new streams are read once more, here
-  auto fill = [&](int k) {   // thread 0: token k of this CTA into slot k % slots
+  // thread 0: token k of this CTA into slot k % slots -- its partial-sum row
+  // (small, so it lands first and its reduction overlaps the stream copy) and
+  // its four stream rows, each on its own barrier
+  auto fill = [&](int k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
     unsigned char *dst = smem + size_t(k % slots) * sbytes;
-    uint64_t *bar = &full[k % slots];
-    tc::mbar_arrive_expect_tx(bar, stream_bytes + part_bytes);
-    tc::bulk_load_hint(dst, p.streams + (size_t)t * HC * H, stream_bytes, bar, read_once);
-    if (part_bytes) tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, bar);
+    if (part_bytes) {
+      tc::mbar_arrive_expect_tx(&pfull[k % slots], part_bytes);
+      tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, &pfull[k % slots]);
+    }
+    tc::mbar_arrive_expect_tx(&sfull[k % slots], stream_bytes);
+    tc::bulk_load_hint(dst, p.streams + (size_t)t * HC * H, stream_bytes, &sfull[k % slots], read_once);
   };
+  // mixes warp: steps 1-2 for token k of this CTA (its pre into pre_s[k & 1])
+  auto token_pre = [&](int k) {
+    const int t = int(blockIdx.x) + k * int(gridDim.x);
+    if (p.pre_in) {
+      // the delayed-mHC consumer: the collapse takes the carried pre-mix
+      if (lane < HC) pre_s[k & 1][lane] = p.pre_in[(size_t)t * HC + lane];
+      return;
+    }
+    if (!tc::mbar_wait_bounded(&pfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) bad = true;
+    const float *part_s = reinterpret_cast<const float *>(smem + size_t(k % slots) * sbytes + stream_bytes);
+    // each of lanes 0-24 sums one value over the groups, in group order
+    float v = 0.f;
+    if (lane < VALUES) {
+#pragma unroll 8
+      for (int g = 0; g < p.slices; ++g) v = __fadd_rn(v, part_s[g * VALUES + lane]);
+    }
+    // the slot's next fill is an async-proxy write after these generic reads
+    tc::fence_proxy_async_smem();
+    const float ss = __shfl_sync(0xffffffffu, v, MIX);
+    const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
+    if (lane < MIX) {
+      const float mix = __fmul_rn(v, rstd);
+      mix_s[k % BATCH][lane] = mix;
+      if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
+      if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
+      if (lane < HC) {
+        const float pre = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+        pre_s[k & 1][lane] = pre;
+        if (p.pre_out) p.pre_out[(size_t)t * HC + lane] = pre;
+      }
+    }
+  };
+
   int filled = 0;   // tokens whose copies were issued (thread 0)
   if (tid == 0)
     for (; filled < slots && filled < n_tok; ++filled) fill(filled);
+  if (warp == MIX_WARP && n_tok > 0) token_pre(0);
 
   const int cols = H / 32;
   for (int k = 0; k < n_tok; ++k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
     unsigned char *slot = smem + size_t(k % slots) * sbytes;
-    if (!tc::mbar_wait_bounded(&full[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) abort_s = 1;
-    const float *part_s = reinterpret_cast<const float *>(slot + stream_bytes);
-
-    // 1.-2. (mixes warp) each of lanes 0-24 sums one value over the groups
-    // in group order; rstd, the mixes, pre (shared with the collapse warps)
-    if (warp == MIX_WARP && p.pre_in) {
-      // the delayed-mHC consumer: the collapse takes the carried pre-mix
-      if (lane < HC) pre_s[lane] = p.pre_in[(size_t)t * HC + lane];
-    } else if (warp == MIX_WARP) {
-      float v = 0.f;
-      if (lane < VALUES)
-        for (int g = 0; g < p.slices; ++g) v = __fadd_rn(v, part_s[g * VALUES + lane]);
-      const float ss = __shfl_sync(0xffffffffu, v, MIX);
-      const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
-      if (lane < MIX) {
-        const float mix = __fmul_rn(v, rstd);
-        mix_s[k % BATCH][lane] = mix;
-        if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
-        if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
-        if (lane < HC) {
-          const float pre = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
-          pre_s[lane] = pre;
-          if (p.pre_out) p.pre_out[(size_t)t * HC + lane] = pre;
-        }
-      }
-    }
-    __syncthreads();
-    if (abort_s) break;
+    // pre of token k is ready; token k - 1 is done with its slot and pre_s
+    // entry.  Every thread takes the same decision: the barrier's own OR of
+    // the threads' failed waits.
+    if (__syncthreads_or(bad)) break;
 
     if (warp == MIX_WARP) {
-      // (fused) post + Sinkhorn per batch of tokens, one token per lane,
-      // beside the batch's last collapse
+      // (fused) post + Sinkhorn per batch of tokens, one token per lane; it
+      // runs before token k + 1's mixes overwrite the batch's first entry
       const int b = k % BATCH;
       if (p.post_out && !p.pre_in && (b == BATCH - 1 || k == n_tok - 1)) {
         const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
         if (lane <= b) post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
         __syncwarp();
       }
+      // steps 1-2 of the next token, beside this token's collapse (its
+      // partial-sum row was issued with its streams, at the last refill)
+      if (k + 1 < n_tok) token_pre(k + 1);
     } else {
       // 3. collapse, kept in registers as BF16; sum of squares of c
+      if (!tc::mbar_wait_bounded(&sfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) bad = true;
       float pre[HC];
 #pragma unroll
-      for (int j = 0; j < HC; ++j) pre[j] = pre_s[j];
+      for (int j = 0; j < HC; ++j) pre[j] = pre_s[k & 1][j];
       const uint16_t *sv = reinterpret_cast<const uint16_t *>(slot);
       uint4 cfr[NF];
       float ssq = 0.f;
@@ -290,8 +314,9 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
       // the slot's next fill is an async-proxy write after these generic reads
       tc::fence_proxy_async_smem();
       asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
-      // the slot has been read: it takes the token `slots` places further on,
-      // whose copies then overlap this token's normalisation
+      // the slot has been read (its partial-sum row by the mixes warp before
+      // this token's first barrier): it takes the token `slots` places further
+      // on, whose copies then overlap this token's normalisation
       if (tid == 0 && filled < n_tok) fill(filled++);
       float sq = 0.f;
 #pragma unroll
@@ -333,8 +358,9 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
         }
       }
     }
-    __syncthreads();
   }
+  if (bad) abort_s = 1;
+  __syncthreads();
   pdl_launch_dependents();
 
   // padding rows of the scale layout: zero their scales (4 columns a store)
@@ -347,8 +373,11 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   if (tid == 0) {
     if (abort_s && p.err) atomicOr(p.err, 2u);
     // copies still in flight land before the CTA may exit
-    for (int k = filled - slots; k < filled; ++k)
-      if (k >= 0) tc::mbar_wait_bounded(&full[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
+    for (int k = filled - slots; k < filled; ++k) {
+      if (k < 0) continue;
+      tc::mbar_wait_bounded(&sfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
+      if (part_bytes) tc::mbar_wait_bounded(&pfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
+    }
   }
 }
 
