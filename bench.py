@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--m", type=int, default=None, help="token count (default: the workload's largest)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-static-weight", action="store_true",
+                    help="read the prenorm weight only after the preceding kernel (not as a layer weight)")
     ap.add_argument("--sweep", action="store_true",
                     help="one line per workload and token count (call time, GB/s, kernel times)")
     return ap.parse_args()
@@ -89,10 +91,17 @@ def call_bytes(w):
     return {"stage": stage, "finish": finish, "mixes": mixes, "total": stage + finish + mixes}
 
 
+# The prenorm weight is a layer weight (MHC_FLAG_STATIC_WEIGHT): each call's
+# stage kernel stages and splits it while the kernel before it finishes.
+STATIC_WEIGHT = True
+
+
 def describe(w):
     return {"workload": w.name, "tokens": w.m, "hidden": w.hidden, "tp": w.tp, "hc": 4,
             "top_k": w.top_k, "moe": w.moe, "mxfp8": w.mxfp8,
             "weight": "none (carried pre)" if w.consume else "bf16 [24][4H]" if w.bf16_fn else "f32 [4H][24]",
+            "weight_staging": ("layer weight: staged while the preceding kernel ends" if STATIC_WEIGHT
+                               else "after the preceding kernel"),
             "residual_only": w.residual_only}
 
 
@@ -286,7 +295,7 @@ def run_ours(args, w):
 
     dev_in = {("norm_weight" if k == "gamma" else k): to_dev(v) for k, v in inputs.items()}
     b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
-                 host_staging=not w.moe, device=local)
+                 host_staging=not w.moe, static_weight=STATIC_WEIGHT, device=local)
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
     nbytes = call_bytes(w)
@@ -410,7 +419,8 @@ def run_sweep(args):
             dev_in = {("norm_weight" if k == "gamma" else k):
                       (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
                        else torch.from_numpy(v)).to(device) for k, v in inputs.items()}
-            b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8)
+            b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
+                         static_weight=STATIC_WEIGHT)
             nbytes = call_bytes(w)
             nsets = 1 if nbytes["total"] >= 3 * l2 else math.ceil(3 * l2 / nbytes["total"]) + 1
             def outputs():
@@ -482,7 +492,9 @@ def run_sweep(args):
 
 
 def main():
+    global STATIC_WEIGHT
     args = parse_args()
+    STATIC_WEIGHT = not args.no_static_weight
     if args.sweep:
         run_sweep(args)
         return

@@ -83,7 +83,16 @@ enum {
    * on the library side stream, so that they overlap whatever the caller
    * enqueues next; post_out / comb_out are then valid only after
    * mhc_boundary_join (or the next call, which joins automatically). */
-  MHC_FLAG_SIDE_MIXES = 1u << 3
+  MHC_FLAG_SIDE_MIXES = 1u << 3,
+  /* The prenorm weight (hc_fn or hc_fn_bf16) is a layer weight: it is written
+   * before the first call, by work the call's stream has already waited for,
+   * and not while calls run.  The stage kernel is a programmatic dependent
+   * launch: its CTAs set up while the kernel before it on the stream is
+   * finishing, and with this flag they also stage the weight and split it
+   * into tensor-core operands then, ahead of the wait for that kernel.  The
+   * partials, streams, post and comb are read only after the wait in any
+   * case.  Results are the same bits with or without the flag. */
+  MHC_FLAG_STATIC_WEIGHT = 1u << 4
 };
 
 /* Construction arguments ([GLM] AllReduceMhcBoundary.__init__, [DSV]

@@ -21,6 +21,7 @@ MHC_FLAG_MXFP8 = 1 << 0
 MHC_FLAG_SYNC_MIXES = 1 << 1
 MHC_FLAG_HOST_STAGING = 1 << 2
 MHC_FLAG_SIDE_MIXES = 1 << 3
+MHC_FLAG_STATIC_WEIGHT = 1 << 4
 
 
 class MhcError(RuntimeError):

@@ -256,6 +256,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.hc_fn = a->hc_fn;
   sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
   sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
+  sp.early_weight = (c.flags & MHC_FLAG_STATIC_WEIGHT) != 0;
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = b->part;
@@ -479,7 +480,8 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   if (c.top_k < 0 || c.top_k > 64) return fail(g_create_error, MHC_ERR_INVALID_ARG, "top_k must be in [0, 64]");
   if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
-  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING | MHC_FLAG_SIDE_MIXES))
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING | MHC_FLAG_SIDE_MIXES |
+                          MHC_FLAG_STATIC_WEIGHT))
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "unknown flag bits 0x%x", c.flags);
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count)

@@ -206,6 +206,9 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
 
   // Nothing below may read the stage kernel's outputs before this point.
   pdl_wait();
+  // The next kernel on the stream may start its own setup on the SMs this
+  // grid leaves free (it waits for this grid before it touches its inputs).
+  pdl_launch_dependents();
 
   const uint64_t read_once = tc::policy_evict_first();   // the new streams are read once more, here
   // thread 0: token k of this CTA into slot k % slots -- its partial-sum row
@@ -361,7 +364,6 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   }
   if (bad) abort_s = 1;
   __syncthreads();
-  pdl_launch_dependents();
 
   // padding rows of the scale layout: zero their scales (4 columns a store)
   if (p.mx_scales) {

@@ -434,8 +434,22 @@ __global__ void __launch_bounds__(NT, 1)
       if (p.fn_terms == 1) tc::tma_prefetch_desc(&tm_fn);
     }
     __syncwarp();
-    // the first group's weight rows before anything else
-    if (gemv) stage_hc_fn(p, &tm_fn, first_group, a_s, bfull);
+    // a layer weight: the first group's rows while the preceding kernel
+    // finishes (nothing before the wait below may read the call's inputs)
+    if (gemv && p.early_weight) stage_hc_fn(p, &tm_fn, first_group, a_s, bfull);
+  } else if (warp == MMA_WARP) {
+    tc::tmem_alloc(slot, TMEM_COLS);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *slot;
+
+  if (warp == PROD_WARP) {
+    // The inputs, and the outputs that the preceding kernel may still read,
+    // are touched only after it has completed.
+    pdl_wait();
+    if (gemv && !p.early_weight) stage_hc_fn(p, &tm_fn, first_group, a_s, bfull);
     for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
     // the later groups' weight rows, so that their staging copies read L2
     const int last_group = gemv ? (u_end - 1) / n_tiles : first_group;
@@ -449,15 +463,6 @@ __global__ void __launch_bounds__(NT, 1)
       }
       __syncwarp();
     }
-  } else if (warp == MMA_WARP) {
-    tc::tmem_alloc(slot, TMEM_COLS);
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *slot;
-
-  if (warp == PROD_WARP) {
     // refill each slot as soon as its previous stage has been read
     int nf = nslot < total_fills ? nslot : total_fills;
     for (; nf < total_fills; ++nf) {
@@ -507,6 +512,16 @@ __global__ void __launch_bounds__(NT, 1)
     const int tl = item / FRAGS, f = item % FRAGS;
     Epi ep = {p.part, p.part_stride, p.m, tmem, mma_bar, abort_s, -1, 0, 0};
     int cur_group = -1, loads = 0;   // hc_fn groups staged so far
+    if (gemv && p.early_weight) {
+      // the first group's B, split while the preceding kernel finishes
+      if (!tc::mbar_wait_bounded(bfull, 0u, WAIT_LIMIT)) *abort_s = 1;
+      ++loads;
+      build_b(p, first_group, a_s, b_s);
+      // every mixer has read the staged rows before any A row is written
+      asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
+      cur_group = first_group;
+    }
+    pdl_wait();
     for (int i = 0; i < n_units; ++i) {
       if (*abort_s) break;
       const int u = u_begin + i, g = u / n_tiles, tile = u % n_tiles;
@@ -642,8 +657,19 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
   const int units = ((p.m + UT - 1) / UT) * p.slices;
   const int grid = units < ctas ? units : ctas;
   const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
-  k_stage_tc<<<grid, NT, smem, stream>>>(p, tm_part, tm_res, tm_post, tm_comb, tm_fn);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs' setup (and, for a layer weight,
+  // its staging and split) overlaps the end of the preceding kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_stage_tc, p, tm_part, tm_res, tm_post, tm_comb, tm_fn);
 }
 
 }  // namespace mhc

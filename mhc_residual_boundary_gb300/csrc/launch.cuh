@@ -44,6 +44,8 @@ struct StageParams {
   const uint16_t *hc_fn_bf16; // [24][4H] bf16 (tensor-core kernel only), or null
   int fn_terms;               // BF16 terms of B: 3 for the FP32 weight, 1 for the BF16 one,
                               // 0 for no GEMV (the delayed-mHC consumer: streams only)
+  int early_weight;           // the weight is a layer weight: stage and split it before
+                              // waiting for the preceding kernel (tensor-core kernel)
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares

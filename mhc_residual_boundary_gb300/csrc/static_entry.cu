@@ -94,8 +94,9 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   if (c.tp < 1 || c.tp > 32) return report(error, error_len, MHC_ERR_INVALID_ARG, "tp must be in [1, 32]");
   if (c.sinkhorn_repeat < 1 || c.sinkhorn_repeat > 10000)
     return report(error, error_len, MHC_ERR_INVALID_ARG, "sinkhorn_repeat must be in [1, 10000]");
-  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES))
-    return report(error, error_len, MHC_ERR_UNSUPPORTED, "only MHC_FLAG_MXFP8 and MHC_FLAG_SYNC_MIXES apply");
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_STATIC_WEIGHT))
+    return report(error, error_len, MHC_ERR_UNSUPPORTED,
+                  "only MHC_FLAG_MXFP8, MHC_FLAG_SYNC_MIXES and MHC_FLAG_STATIC_WEIGHT apply");
   if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
     return report(error, error_len, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
 
@@ -163,6 +164,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.hc_fn = a->hc_fn;
   sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
   sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
+  sp.early_weight = (c.flags & MHC_FLAG_STATIC_WEIGHT) != 0;
   sp.residual_out = static_cast<uint16_t *>(a->residual_out);
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;

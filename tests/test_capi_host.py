@@ -103,3 +103,11 @@ def test_null_handle_calls_fail_cleanly(capi):
     assert lib.mhc_boundary_join(None, None) == 1
     assert lib.mhc_boundary_destroy(None) == 0
     assert lib.mhc_boundary_launches_per_call(None) == 0
+
+
+def test_flag_values_match_the_header(capi):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    declared = {name: 1 << int(bit) for name, bit in re.findall(r"\b(MHC_FLAG_[A-Z0-9_]+)\s*=\s*1u\s*<<\s*(\d+)", text)}
+    assert declared, "no flags found in the header"
+    bound = {name: getattr(capi, name) for name in dir(capi) if name.startswith("MHC_FLAG_")}
+    assert declared == bound

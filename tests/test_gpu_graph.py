@@ -16,13 +16,14 @@ def _bytes(outs):
     return {k: v.view(torch.uint8).cpu().numpy() for k, v in outs.items()}
 
 
-@pytest.mark.parametrize("side_mixes", [False, True])
-def test_captured_calls_match_eager_calls(side_mixes):
+@pytest.mark.parametrize("side_mixes,static_weight", [(False, False), (True, False), (False, True)])
+def test_captured_calls_match_eager_calls(side_mixes, static_weight):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     from mhc_residual_boundary_gb300 import Boundary
     hidden, tp, m = 2048, 4, 40
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, mxfp8=True, side_mixes=side_mixes)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, mxfp8=True, side_mixes=side_mixes,
+                 static_weight=static_weight)
     try:
         ins = [to_device(synth.make_inputs(hidden, tp, m, seed=s)) for s in (31, 32)]
         eager = []

@@ -22,7 +22,7 @@ def Boundary():
 
 
 def check(Boundary, hidden, tp, m, *, seed=0, moe=False, top_k=0, mxfp8=False, holes=0.0,
-          capacity=None, mutate=None, bf16_weight=False, **cfg):
+          capacity=None, mutate=None, bf16_weight=False, flags=None, **cfg):
     inp = synth.make_inputs(hidden, tp, m, top_k=top_k, moe=moe, seed=seed, holes=holes)
     if bf16_weight:
         # the GLM page's form of the weight, BF16 [24][4H], instead of hc_fn
@@ -31,7 +31,8 @@ def check(Boundary, hidden, tp, m, *, seed=0, moe=False, top_k=0, mxfp8=False, h
         mutate(inp)
     p = oracle.Problem(hidden, tp, m, top_k=top_k, rows_per_rank=m * top_k if moe else 0, **cfg)
     ref = oracle_outputs(p, inp, moe=moe, mxfp8=mxfp8)
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=capacity or m, top_k=top_k, mxfp8=mxfp8, **cfg)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=capacity or m, top_k=top_k, mxfp8=mxfp8,
+                 **(flags or {}), **cfg)
     try:
         got = run_gpu(b, inp, moe=moe, mxfp8=mxfp8)
         b.check_errors()
@@ -119,7 +120,45 @@ def test_other_scalars(Boundary):
           norm_eps=1e-2, seed=9)
 
 
-MIXES_PLACEMENTS = {"fused": {}, "side": {"side_mixes": True}, "sync": {"sync_mixes": True}}
+@pytest.mark.parametrize("hidden,tp,m,bf16,moe", [(5120, 4, 4, False, False), (6144, 8, 300, False, False),
+                                                  (2048, 3, 1024, False, False), (6144, 4, 64, True, False),
+                                                  (1024, 4, 60, False, True)])
+def test_static_weight(Boundary, hidden, tp, m, bf16, moe):
+    # the weight staged and split before the stage kernel waits for the
+    # kernel ahead of it: same results
+    check(Boundary, hidden, tp, m, bf16_weight=bf16, moe=moe, top_k=4 if moe else 0,
+          mxfp8=hidden % 128 == 0, flags={"static_weight": True}, seed=hidden + m)
+
+
+def test_static_weight_chained_calls_match(Boundary):
+    # each call reads the previous call's residual_out, post_out and comb_out
+    # on the same stream, while its stage kernel may start during the
+    # previous finish kernel: the chain gives the bits of the chain without
+    # the early staging
+    hidden, tp, m, calls = 2048, 4, 48, 12
+    inp = to_device(synth.make_inputs(hidden, tp, m, seed=21))
+    results = {}
+    for static in (False, True):
+        b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, static_weight=static)
+        cur, outs = dict(inp), []
+        for _ in range(calls):
+            o = b.empty_outputs(m, extras=True)
+            b.run(cur, o)
+            outs.append(o)
+            cur = dict(cur)
+            cur["residual"], cur["post"], cur["comb"] = o["residual_out"], o["post_out"], o["comb_out"]
+        b.join()
+        torch.cuda.synchronize()
+        b.check_errors()
+        results[static] = [to_numpy(o) for o in outs]
+        b.close()
+    for i, (a, c) in enumerate(zip(results[False], results[True])):
+        for name in a:
+            assert np.array_equal(a[name], c[name]), (i, name)
+
+
+MIXES_PLACEMENTS = {"fused": {}, "side": {"side_mixes": True}, "sync": {"sync_mixes": True},
+                    "static": {"static_weight": True}}
 
 
 def test_mixes_placements_give_same_bits(Boundary):
@@ -132,7 +171,7 @@ def test_mixes_placements_give_same_bits(Boundary):
         outs[name] = run_gpu(b, inp)
         b.close()
     for name in outs["fused"]:
-        for other in ("side", "sync"):
+        for other in ("side", "sync", "static"):
             assert np.array_equal(outs["fused"][name], outs[other][name]), (name, other)
 
 
