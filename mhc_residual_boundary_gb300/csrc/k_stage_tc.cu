@@ -387,8 +387,23 @@ __global__ void __launch_bounds__(NT, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (p.m + UT - 1) / UT;
   const int units = n_tiles * p.slices;
-  const int u_begin = int((long long)blockIdx.x * units / gridDim.x);
-  const int u_end = int((long long)(blockIdx.x + 1) * units / gridDim.x);
+  // Units are numbered group-major.  Either each CTA takes a contiguous
+  // share of them, or (group_aligned) the C CTAs are shared out over the G
+  // groups -- group g gets CTAs floor(g * C / G) .. floor((g + 1) * C / G) - 1
+  // -- and each takes a contiguous share of its group's tiles, so that no CTA
+  // splits a second weight group.
+  int u_begin, u_end;
+  if (p.group_aligned) {
+    const long long G = p.slices, C = gridDim.x;
+    const int g = int(((long long)(blockIdx.x + 1) * G - 1) / C);
+    const int c0 = int(g * C / G), c1 = int((g + 1) * C / G);
+    const int k = int(blockIdx.x) - c0, n = c1 - c0;
+    u_begin = g * n_tiles + int((long long)k * n_tiles / n);
+    u_end = g * n_tiles + int((long long)(k + 1) * n_tiles / n);
+  } else {
+    u_begin = int((long long)blockIdx.x * units / gridDim.x);
+    u_end = int((long long)(blockIdx.x + 1) * units / gridDim.x);
+  }
   const int n_units = u_end - u_begin;             // >= 1: the grid is at most `units`
   const int nslot = ring_slots(p.tp, p.fn_terms), sbytes = slot_bytes(p.tp);
   const int total_fills = n_units * NSTAGE;
@@ -654,8 +669,18 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
     if (!encode(&tm_fn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.hc_fn_bf16, fn_dims, fn_strides, fn_box))
       return cudaErrorInvalidValue;
   }
-  const int units = ((p.m + UT - 1) / UT) * p.slices;
+  // One unit per CTA when there are no more units than CTAs; else the
+  // group-aligned split when it gives no CTA more units than the contiguous
+  // one (with several units a CTA, mostly at small m, a CTA that straddles two
+  // groups would stage and split a second weight group on its critical path).
+  const int tiles = (p.m + UT - 1) / UT, units = tiles * p.slices;
   const int grid = units < ctas ? units : ctas;
+  StageParams q = p;
+  q.group_aligned = 0;
+  if (units > ctas && ctas >= p.slices && p.fn_terms > 0) {
+    const int per = ctas / p.slices;   // fewest CTAs any group gets
+    q.group_aligned = (tiles + per - 1) / per <= (units + ctas - 1) / ctas;
+  }
   const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
   // programmatic dependent launch: the CTAs' setup (and, for a layer weight,
   // its staging and split) overlaps the end of the preceding kernel
@@ -669,7 +694,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_stage_tc, p, tm_part, tm_res, tm_post, tm_comb, tm_fn);
+  return cudaLaunchKernelEx(&cfg, k_stage_tc, q, tm_part, tm_res, tm_post, tm_comb, tm_fn);
 }
 
 }  // namespace mhc

@@ -46,6 +46,7 @@ struct StageParams {
                               // 0 for no GEMV (the delayed-mHC consumer: streams only)
   int early_weight;           // the weight is a layer weight: stage and split it before
                               // waiting for the preceding kernel (tensor-core kernel)
+  int group_aligned;          // set by the launcher: every CTA's units lie in one column group
   uint16_t *residual_out;     // [m][4][H]
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares
