@@ -30,7 +30,11 @@
 //     relative) so that each BF16 x BF16 product is exact and the sum
 //     accumulates in FP32 in tensor memory: 3 x 8 MMAs of M=128, N=96, K=16
 //     into one of two accumulators (by unit parity).
-//   epilogue (one unit later, so that it overlaps the next unit's loads):
+//   order of a mixer iteration: post-mix of unit i, wait for unit i - 1's
+//     MMAs, A rows of unit i to shared memory and to the MMA warp, then --
+//     while those MMAs run -- the global stores of unit i and the epilogue
+//     of unit i - 1.
+//   epilogue (one unit later):
 //     warp w reads TMEM lane quarter w % 4 (the rows of stage w % 4's
 //     tokens, four lanes per token) and six of the 24 outputs of all four
 //     stream blocks; each lane keeps its own stream's block and the four
@@ -555,19 +559,23 @@ __global__ void __launch_bounds__(NT, 1)
       uint4 yb, nv[HC];
       float ss = mix_item(it, yb, nv);
       const int t = tile * UT + q * QT + tl, h = g * UK + f * VEC;
-      if (t < p.m && h < p.hidden) {
-        if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
+      const bool live = t < p.m && h < p.hidden;
+      if (!gemv) {
+        if (live) {
+          if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
 #pragma unroll
-        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
+          for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
+        }
+        continue;
       }
-      if (!gemv) continue;
-      // the A buffer is free once the previous unit's MMAs are done
-      if (ep.i >= 0) epilogue(ep);
-      ep.i = -1;
+      // The A buffer (and B) are free once the previous unit's MMAs are done.
+      if (i > 0 && !tc::mbar_wait_bounded(&mma_bar[(i - 1) & 1], uint32_t(((i - 1) >> 1) & 1), WAIT_LIMIT)) {
+        *abort_s = 1;
+        break;
+      }
       if (g != cur_group) {
-        // B and the A space change (the previous unit's MMAs are done); the
-        // first group's rows were staged at kernel start, so their split
-        // overlaps the first unit's loads and post-mix
+        // B and the A space change; the first group's rows were staged at
+        // kernel start, so their split overlaps the first unit's loads
         if (cur_group >= 0 && warp == 0) stage_hc_fn(p, &tm_fn, g, a_s, bfull);
         if (!tc::mbar_wait_bounded(bfull, uint32_t(loads & 1), WAIT_LIMIT)) {
           *abort_s = 1;
@@ -584,17 +592,25 @@ __global__ void __launch_bounds__(NT, 1)
         const int row = 32 * q + 4 * tl + j;
         *reinterpret_cast<uint4 *>(a_s + f * A_KCOL + (row >> 3) * 128 + (row & 7) * 16) = nv[j];
       }
-      // the 16 fragments of a token are 16 consecutive lanes
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-      if (f == 0 && t < p.m) p.part[(size_t)t * p.part_stride + g * VALUES + MIX] = ss;
       // hand the A rows (and a new B) to the tensor core
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(afull);
+      // while the tensor core runs: the global stores, the token's sum of
+      // squares (its 16 fragments are 16 consecutive lanes) and the previous
+      // unit's sums (its MMAs are done: waited for above)
+      if (live) {
+        if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
+#pragma unroll
+        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+      if (f == 0 && t < p.m) p.part[(size_t)t * p.part_stride + g * VALUES + MIX] = ss;
+      if (ep.i >= 0) epilogue(ep);
       ep.i = i;
       ep.tile = tile;
       ep.group = g;
