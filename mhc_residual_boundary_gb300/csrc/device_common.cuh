@@ -51,6 +51,15 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return v;
 }
 
+// Read-only 16-byte read, cached in L1 (data no kernel of the call writes
+// and the CTA re-reads, such as a weight).  Not ordered after the thread's
+// own earlier stores, so independent reads issue back to back.
+__device__ __forceinline__ uint4 ld_ro(const void *p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
 // Plain 16-byte read through L1 (data other threads of the CTA re-read).
 __device__ __forceinline__ uint4 ld_vec(const void *p) {
   return *reinterpret_cast<const uint4 *>(p);

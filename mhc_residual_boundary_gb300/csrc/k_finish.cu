@@ -175,8 +175,11 @@ __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const flo
 }
 
 // NF: 16-byte fragments of a row per collapse thread (ceil(H / 8 / 224)).
+// The register bound follows the CTAs per SM that the shared memory allows
+// at that width (a slot is 8H bytes and more): 4 up to NF = 5, then 3, 2, 1.
 template <int NF>
-__global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slots) {
+__global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 1)
+    k_finish(const FinishParams p, int slots) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t sfull[MAX_SLOTS];   // a slot's four stream rows arrived
   __shared__ __align__(8) uint64_t pfull[MAX_SLOTS];   // a slot's partial-sum row arrived
@@ -211,19 +214,25 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   pdl_launch_dependents();
 
   const uint64_t read_once = tc::policy_evict_first();   // the new streams are read once more, here
-  // thread 0: token k of this CTA into slot k % slots -- its partial-sum row
-  // (small, so it lands first and its reduction overlaps the stream copy) and
-  // its four stream rows, each on its own barrier
-  auto fill = [&](int k) {
+  // Token k of this CTA goes to slot k % slots, on two barriers: its four
+  // stream rows (thread 0, once the collapse has read the slot) and its
+  // partial-sum row (the mixes warp, once it has reduced the row that the
+  // slot held before; a token earlier, so that the copy is hidden).
+  auto fill_streams = [&](int k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
-    unsigned char *dst = smem + size_t(k % slots) * sbytes;
-    if (part_bytes) {
-      tc::mbar_arrive_expect_tx(&pfull[k % slots], part_bytes);
-      tc::bulk_load(dst + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes, &pfull[k % slots]);
-    }
     tc::mbar_arrive_expect_tx(&sfull[k % slots], stream_bytes);
-    tc::bulk_load_hint(dst, p.streams + (size_t)t * HC * H, stream_bytes, &sfull[k % slots], read_once);
+    tc::bulk_load_hint(smem + size_t(k % slots) * sbytes, p.streams + (size_t)t * HC * H, stream_bytes,
+                       &sfull[k % slots], read_once);
   };
+  auto fill_part = [&](int k) {
+    const int t = int(blockIdx.x) + k * int(gridDim.x);
+    tc::mbar_arrive_expect_tx(&pfull[k % slots], part_bytes);
+    tc::bulk_load(smem + size_t(k % slots) * sbytes + stream_bytes, p.part + (size_t)t * p.part_stride, part_bytes,
+                  &pfull[k % slots]);
+  };
+  // partial-sum rows (mixes warp): copies issued for tokens < pissued, rows
+  // reduced for tokens < preduced
+  int pissued = part_bytes ? (slots < n_tok ? slots : n_tok) : 0, preduced = 0;
   // mixes warp: steps 1-2 for token k of this CTA (its pre into pre_s[k & 1])
   auto token_pre = [&](int k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
@@ -240,8 +249,14 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
 #pragma unroll 8
       for (int g = 0; g < p.slices; ++g) v = __fadd_rn(v, part_s[g * VALUES + lane]);
     }
-    // the slot's next fill is an async-proxy write after these generic reads
+    // the row's next fill is an async-proxy write after these generic reads
     tc::fence_proxy_async_smem();
+    __syncwarp();
+    preduced = k + 1;
+    if (k + slots < n_tok) {
+      if (lane == 0) fill_part(k + slots);
+      pissued = k + slots + 1;
+    }
     const float ss = __shfl_sync(0xffffffffu, v, MIX);
     const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
     if (lane < MIX) {
@@ -257,9 +272,12 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
     }
   };
 
-  int filled = 0;   // tokens whose copies were issued (thread 0)
+  int filled = 0;   // tokens whose stream copies were issued (thread 0)
   if (tid == 0)
-    for (; filled < slots && filled < n_tok; ++filled) fill(filled);
+    for (; filled < slots && filled < n_tok; ++filled) {
+      if (part_bytes) fill_part(filled);
+      fill_streams(filled);
+    }
   if (warp == MIX_WARP && n_tok > 0) token_pre(0);
 
   const int cols = H / 32;
@@ -312,15 +330,20 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
           for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
         }
       }
+      // the norm weight's fragments, all requested before any store of this
+      // token, so that they cost one round trip, overlapping the reduction
+      uint4 gw[NF];
+#pragma unroll
+      for (int i = 0; i < NF; ++i)
+        gw[i] = tid + i * CT < nfrag ? ld_ro(p.gamma + (size_t)(tid + i * CT) * VEC) : make_uint4(0u, 0u, 0u, 0u);
       ssq = warp_sum(ssq);
       if (lane == 0) red_s[warp] = ssq;
       // the slot's next fill is an async-proxy write after these generic reads
       tc::fence_proxy_async_smem();
       asm volatile("bar.sync 1, %0;" ::"n"(CT) : "memory");
-      // the slot has been read (its partial-sum row by the mixes warp before
-      // this token's first barrier): it takes the token `slots` places further
-      // on, whose copies then overlap this token's normalisation
-      if (tid == 0 && filled < n_tok) fill(filled++);
+      // the slot's stream rows have been read: they take the token `slots`
+      // places further on, whose copy then overlaps this token's normalisation
+      if (tid == 0 && filled < n_tok) fill_streams(filled++);
       float sq = 0.f;
 #pragma unroll
       for (int w = 0; w < CWARPS; ++w) sq += red_s[w];
@@ -335,7 +358,7 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
         if (live) {
           float c[8], g[8];
           unpack8(cfr[i], c);
-          unpack8(ld_vec(p.gamma + (size_t)fr * VEC), g);
+          unpack8(gw[i], g);
 #pragma unroll
           for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(c[e], ir), g[e]);
           st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, round8(o));
@@ -374,12 +397,16 @@ __global__ void __launch_bounds__(NT, 4) k_finish(const FinishParams p, int slot
   }
   if (tid == 0) {
     if (abort_s && p.err) atomicOr(p.err, 2u);
-    // copies still in flight land before the CTA may exit
+    // stream copies still in flight land before the CTA may exit
     for (int k = filled - slots; k < filled; ++k) {
       if (k < 0) continue;
       tc::mbar_wait_bounded(&sfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
-      if (part_bytes) tc::mbar_wait_bounded(&pfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
     }
+  }
+  if (warp == MIX_WARP && lane == 0) {
+    // partial-sum rows copied but not reduced (only after a failed wait)
+    for (int k = preduced; k < pissued; ++k)
+      tc::mbar_wait_bounded(&pfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT);
   }
 }
 
