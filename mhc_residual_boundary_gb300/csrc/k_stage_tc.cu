@@ -76,8 +76,12 @@ constexpr int QT = 8;                         // tokens per pipeline stage
 constexpr int NSTAGE = UT / QT;               // stages per unit
 constexpr int STAGE_WARPS = MIX_WARPS / NSTAGE;   // mixer warps per stage
 constexpr int FRAGS = UK / VEC;               // 16-byte fragments per row piece
-constexpr int A_KCOL = ROWS * 16 + 16;        // bytes between A core columns (+16: fewer bank conflicts)
-constexpr int A_BYTES = KCOLS * A_KCOL;
+// A: two halves of 64 columns, each 128 rows of 128 bytes in the 128-byte
+// swizzled K-major layout (16-byte chunk c of row r at chunk c ^ (r % 8)),
+// which the tensor core reads and a swizzled TMA store writes out as is.
+constexpr int A_ROW = 128;                    // bytes of one row of a half
+constexpr int A_HALF = ROWS * A_ROW;          // 16 KB
+constexpr int A_BYTES = 2 * A_HALF;
 constexpr int B_KCOL = UN * 16;               // bytes between B core columns
 constexpr int TERM_BYTES = KCOLS * B_KCOL;    // one BF16 term of B
 constexpr int B_BYTES = 3 * TERM_BYTES;       // FP32 weight: hi, mid, lo
@@ -110,9 +114,11 @@ struct Layout {
   static constexpr int bfull = mma + 16;                // uint64: a group's hc_fn rows staged
   static constexpr int slot = bfull + 8;                // TMEM address
   static constexpr int abort = slot + 4;                // int
-  static constexpr int b = 256;
+  static constexpr int b = 1024;
   static_assert(abort + 4 <= b, "control block");
-  static_assert(b % 128 == 0 && TERM_BYTES % 128 == 0 && A_BYTES % 128 == 0, "TMA / MMA alignment");
+  // A (after B) starts on a 1024-byte boundary: the swizzle pattern repeats
+  // every 8 rows of 128 bytes
+  static_assert(b % 1024 == 0 && TERM_BYTES % 1024 == 0 && A_BYTES % 128 == 0, "TMA / MMA alignment");
 };
 __host__ __device__ constexpr int layout_a(int terms) { return Layout::b + terms * TERM_BYTES; }
 __host__ __device__ constexpr int layout_ring(int terms) {
@@ -375,7 +381,8 @@ __device__ __forceinline__ float mix_item(Item &it, uint4 &yb, uint4 (&nv)[HC]) 
 __global__ void __launch_bounds__(NT, 1)
     k_stage_tc(const StageParams p, const __grid_constant__ CUtensorMap tm_part,
                const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_post,
-               const __grid_constant__ CUtensorMap tm_comb, const __grid_constant__ CUtensorMap tm_fn) {
+               const __grid_constant__ CUtensorMap tm_comb, const __grid_constant__ CUtensorMap tm_fn,
+               const __grid_constant__ CUtensorMap tm_out) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Layout::full);
   uint64_t *empty = reinterpret_cast<uint64_t *>(smem + Layout::empty);
@@ -451,6 +458,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::tma_prefetch_desc(&tm_post);
       tc::tma_prefetch_desc(&tm_comb);
       if (p.fn_terms == 1) tc::tma_prefetch_desc(&tm_fn);
+      if (gemv) tc::tma_prefetch_desc(&tm_out);
     }
     __syncwarp();
     // a layer weight: the first group's rows while the preceding kernel
@@ -499,7 +507,8 @@ __global__ void __launch_bounds__(NT, 1)
   } else if (warp == MMA_WARP) {
     // a unit's 3 x 8 MMAs once its A operand is complete
     const uint32_t idesc = tc::idesc_bf16_f32(ROWS, UN);
-    const uint64_t a0 = tc::smem_desc(tc::smem_addr(a_s), A_KCOL, 128);
+    // A: 128-byte swizzle (layout type 2), 8-row groups 1024 bytes apart
+    const uint64_t a0 = tc::smem_desc(tc::smem_addr(a_s), 16, 8 * A_ROW) | (uint64_t(2) << 61);
     const uint64_t b0 = tc::smem_desc(tc::smem_addr(b_s), B_KCOL, 128);
     int nm = 0;
     for (; gemv && nm < n_units; ++nm) {
@@ -514,17 +523,29 @@ __global__ void __launch_bounds__(NT, 1)
         for (int term = 0; term < p.fn_terms; ++term) {
 #pragma unroll
           for (int ks = 0; ks < UK / 16; ++ks) {
-            const uint64_t ad = a0 + uint64_t((2 * ks * A_KCOL) >> 4);
+            // K step ks: half ks / 4, byte 32 * (ks % 4) of the swizzled row
+            const uint64_t ad = a0 + uint64_t(((ks >> 2) * A_HALF + (ks & 3) * 32) >> 4);
             const uint64_t bd = b0 + uint64_t(((term * KCOLS + 2 * ks) * B_KCOL) >> 4);
             tc::mma_bf16(d, ad, bd, idesc, (term | ks) != 0);
           }
         }
+        // the unit's new streams, A as it stands, to residual_out: one
+        // swizzled tensor store per half (rows past m, columns past H are
+        // not written); A is released (the MMA barrier) only after both
+        // stores have read it
+        const int u = u_begin + nm, h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT;
+        tc::tma_store_3d(&tm_out, a_s, h0, 0, t0);
+        if (h0 + UK / 2 < p.hidden) tc::tma_store_3d(&tm_out, a_s + A_HALF, h0 + UK / 2, 0, t0);
+        tc::bulk_commit_group();
+        tc::bulk_wait_read_all();
         tc::mma_commit(&mma_bar[nm & 1]);
       }
       __syncwarp();
     }
-    // issued MMAs complete before the tensor memory is released
+    // issued MMAs complete before the tensor memory is released, and the
+    // stores before the CTA exits
     if (nm > 0) tc::mbar_wait_bounded(&mma_bar[(nm - 1) & 1], uint32_t(((nm - 1) >> 1) & 1), WAIT_LIMIT);
+    if (tc::elect_one()) tc::bulk_wait_all();
     __syncwarp();
   } else {
     const int q = warp / STAGE_WARPS, item = (warp % STAGE_WARPS) * 32 + lane;
@@ -590,21 +611,18 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
       for (int j = 0; j < HC; ++j) {
         const int row = 32 * q + 4 * tl + j;
-        *reinterpret_cast<uint4 *>(a_s + f * A_KCOL + (row >> 3) * 128 + (row & 7) * 16) = nv[j];
+        *reinterpret_cast<uint4 *>(a_s + (f >> 3) * A_HALF + row * A_ROW + (((f & 7) ^ (row & 7)) << 4)) = nv[j];
       }
       // hand the A rows (and a new B) to the tensor core
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(afull);
-      // while the tensor core runs: the global stores, the token's sum of
-      // squares (its 16 fragments are 16 consecutive lanes) and the previous
-      // unit's sums (its MMAs are done: waited for above)
-      if (live) {
-        if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
-#pragma unroll
-        for (int j = 0; j < HC; ++j) st_vec(p.residual_out + ((size_t)t * HC + j) * p.hidden + h, nv[j]);
-      }
+      // while the tensor core runs (and the MMA warp stores the new streams
+      // from A): the stage-1 sum if asked for, the token's sum of squares (its
+      // 16 fragments are 16 consecutive lanes) and the previous unit's sums
+      // (its MMAs are done: waited for above)
+      if (live && p.reduced_out) st_vec(p.reduced_out + (size_t)t * p.hidden + h, yb);
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       ss += __shfl_xor_sync(0xffffffffu, ss, 4);
@@ -640,12 +658,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base, const cuuint64_t *dims,
-            const cuuint64_t *strides, const cuuint32_t *box) {
+            const cuuint64_t *strides, const cuuint32_t *box,
+            CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   const cuuint32_t ones[3] = {1, 1, 1};
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   return fn(map, type, cuuint32_t(rank), const_cast<void *>(base), dims, strides, box, ones,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -664,7 +683,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
   if (!(p.fn_terms == 3 && p.hc_fn) && !(p.fn_terms == 1 && p.hc_fn_bf16) && p.fn_terms != 0)
     return cudaErrorInvalidValue;
   const cuuint64_t H = cuuint64_t(p.hidden), M = cuuint64_t(p.m), TP = cuuint64_t(p.tp);
-  CUtensorMap tm_part, tm_res, tm_post, tm_comb, tm_fn = {};
+  CUtensorMap tm_part, tm_res, tm_post, tm_comb, tm_fn = {}, tm_out = {};
   const cuuint64_t part_dims[3] = {H, M, TP}, part_strides[2] = {H * 2, M * H * 2};
   const cuuint32_t part_box[3] = {UK, QT, cuuint32_t(p.tp)};
   const cuuint64_t res_dims[3] = {H, HC, M}, res_strides[2] = {H * 2, HC * H * 2};
@@ -678,6 +697,14 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
       !encode(&tm_post, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.post, post_dims, post_strides, post_box) ||
       !encode(&tm_comb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.comb, comb_dims, comb_strides, comb_box))
     return cudaErrorInvalidValue;
+  if (p.fn_terms > 0) {
+    // residual_out [m][4][H], written from A: box of 64 columns x 4 streams x
+    // 32 tokens, 128-byte swizzle (one half of A)
+    const cuuint32_t out_box[3] = {UK / 2, HC, UT};
+    if (!encode(&tm_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.residual_out, res_dims, res_strides, out_box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   if (p.fn_terms == 1) {
     // the BF16 weight [24][4H]: box of 128 columns x 24 rows (one stream of a group)
     const cuuint64_t fn_dims[2] = {HC * H, MIX}, fn_strides[1] = {HC * H * 2};
@@ -710,7 +737,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_stage_tc, q, tm_part, tm_res, tm_post, tm_comb, tm_fn);
+  return cudaLaunchKernelEx(&cfg, k_stage_tc, q, tm_part, tm_res, tm_post, tm_comb, tm_fn, tm_out);
 }
 
 }  // namespace mhc
