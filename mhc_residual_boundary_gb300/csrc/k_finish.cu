@@ -92,6 +92,16 @@ __device__ __forceinline__ float inv_scale(uint32_t e) {
   return e < 254u ? __uint_as_float((254u - e) << 23) : __uint_as_float(0x00400000u);
 }
 
+// A BF16 pair as FP32 (exact).
+__device__ __forceinline__ float2 pair(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
+// Lane-wise maximum of two BF16 pairs (finite, non-negative here).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   unsigned short lo, hi;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
@@ -304,32 +314,38 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
     } else {
       // 3. collapse, kept in registers as BF16; sum of squares of c
       if (!tc::mbar_wait_bounded(&sfull[k % slots], uint32_t(k / slots) & 1u, WAIT_LIMIT)) bad = true;
-      float pre[HC];
+      // on element pairs (FP32x2): c = (n0 * pre0 + n1 * pre1) + (n2 * pre2 +
+      // n3 * pre3), each product and sum rounded on its own
+      float2 pre2[HC];
 #pragma unroll
-      for (int j = 0; j < HC; ++j) pre[j] = pre_s[k & 1][j];
+      for (int j = 0; j < HC; ++j) pre2[j] = make_float2(pre_s[k & 1][j], pre_s[k & 1][j]);
       const uint16_t *sv = reinterpret_cast<const uint16_t *>(slot);
       uint4 cfr[NF];
-      float ssq = 0.f;
+      float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < NF; ++i) {
         const int fr = tid + i * CT;
         cfr[i] = make_uint4(0u, 0u, 0u, 0u);
         if (fr < nfrag) {
-          float n0[8], n1[8], n2[8], n3[8], c[8];
           const uint16_t *s = sv + (size_t)fr * VEC;
-          unpack8(*reinterpret_cast<const uint4 *>(s), n0);
-          unpack8(*reinterpret_cast<const uint4 *>(s + H), n1);
-          unpack8(*reinterpret_cast<const uint4 *>(s + 2 * H), n2);
-          unpack8(*reinterpret_cast<const uint4 *>(s + 3 * H), n3);
+          const uint4 w0 = *reinterpret_cast<const uint4 *>(s), w1 = *reinterpret_cast<const uint4 *>(s + H);
+          const uint4 w2 = *reinterpret_cast<const uint4 *>(s + 2 * H), w3 = *reinterpret_cast<const uint4 *>(s + 3 * H);
+          const uint32_t n0[4] = {w0.x, w0.y, w0.z, w0.w}, n1[4] = {w1.x, w1.y, w1.z, w1.w};
+          const uint32_t n2[4] = {w2.x, w2.y, w2.z, w2.w}, n3[4] = {w3.x, w3.y, w3.z, w3.w};
+          uint32_t c[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            c[e] = __fadd_rn(__fadd_rn(__fmul_rn(n0[e], pre[0]), __fmul_rn(n1[e], pre[1])),
-                             __fadd_rn(__fmul_rn(n2[e], pre[2]), __fmul_rn(n3[e], pre[3])));
-          cfr[i] = round8(c);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) ssq = fmaf(c[e], c[e], ssq);
+          for (int e = 0; e < 4; ++e) {
+            const float2 a = __fadd2_rn(__fmul2_rn(pair(n0[e]), pre2[0]), __fmul2_rn(pair(n1[e]), pre2[1]));
+            const float2 b = __fadd2_rn(__fmul2_rn(pair(n2[e]), pre2[2]), __fmul2_rn(pair(n3[e]), pre2[3]));
+            const float2 v = __fadd2_rn(a, b);
+            c[e] = pack_bf16x2(v.x, v.y);
+            const float2 r = pair(c[e]);   // the rounded value, as stored
+            ss2 = __ffma2_rn(r, r, ss2);
+          }
+          cfr[i] = make_uint4(c[0], c[1], c[2], c[3]);
         }
       }
+      float ssq = __fadd_rn(ss2.x, ss2.y);
       // the norm weight's fragments, all requested before any store of this
       // token, so that they cost one round trip, overlapping the reduction
       uint4 gw[NF];
@@ -349,35 +365,39 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
       for (int w = 0; w < CWARPS; ++w) sq += red_s[w];
       const float ir = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(sq, float(H)), p.norm_eps)));
 
-      // 4. normalise, store, optional MXFP8 (4 consecutive lanes = one block)
+      // 4. normalise (pairs: (c * inv_rms) * gamma), store, optional MXFP8
+      // (4 consecutive lanes = one 32-element block)
+      const float2 ir2 = make_float2(ir, ir);
 #pragma unroll
       for (int i = 0; i < NF; ++i) {
         const int fr = tid + i * CT;
         const bool live = fr < nfrag;
-        float o[8];
+        const uint32_t cw[4] = {cfr[i].x, cfr[i].y, cfr[i].z, cfr[i].w};
+        const uint32_t gv[4] = {gw[i].x, gw[i].y, gw[i].z, gw[i].w};
+        uint32_t ow[4] = {0u, 0u, 0u, 0u};   // the output as stored (BF16 pairs); 0 for no fragment
         if (live) {
-          float c[8], g[8];
-          unpack8(cfr[i], c);
-          unpack8(gw[i], g);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(__fmul_rn(c[e], ir), g[e]);
-          st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, round8(o));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const float2 o = __fmul2_rn(__fmul2_rn(pair(cw[e]), ir2), pair(gv[e]));
+            ow[e] = pack_bf16x2(o.x, o.y);
+          }
+          st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, make_uint4(ow[0], ow[1], ow[2], ow[3]));
         }
         if (p.mx_values) {
-          float amax = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(o[e]));
+          // the block's largest magnitude, on the stored BF16 pairs
+          const uint32_t m2 = bf16x2_max(bf16x2_max(ow[0] & 0x7fff7fffu, ow[1] & 0x7fff7fffu),
+                                         bf16x2_max(ow[2] & 0x7fff7fffu, ow[3] & 0x7fff7fffu));
+          float amax = fmaxf(bf16_lo(m2), bf16_hi(m2));
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
           const uint32_t e8 = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
-          const float inv = inv_scale(e8);
+          const float2 inv2 = make_float2(inv_scale(e8), inv_scale(e8));
           if (live) {
+            const float2 q0 = __fmul2_rn(pair(ow[0]), inv2), q1 = __fmul2_rn(pair(ow[1]), inv2);
+            const float2 q2 = __fmul2_rn(pair(ow[2]), inv2), q3 = __fmul2_rn(pair(ow[3]), inv2);
             uint2 q;
-            q.x = e4m3x4(__fmul_rn(o[0], inv), __fmul_rn(o[1], inv), __fmul_rn(o[2], inv), __fmul_rn(o[3], inv));
-            q.y = e4m3x4(__fmul_rn(o[4], inv), __fmul_rn(o[5], inv), __fmul_rn(o[6], inv), __fmul_rn(o[7], inv));
+            q.x = e4m3x4(q0.x, q0.y, q1.x, q1.y);
+            q.y = e4m3x4(q2.x, q2.y, q3.x, q3.y);
             *reinterpret_cast<uint2 *>(p.mx_values + (size_t)t * H + (size_t)fr * VEC) = q;
             if ((fr & 3) == 0) p.mx_scales[swizzle_128x4(t, fr / 4, cols)] = uint8_t(e8);
           }

@@ -712,17 +712,22 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
     if (!encode(&tm_fn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.hc_fn_bf16, fn_dims, fn_strides, fn_box))
       return cudaErrorInvalidValue;
   }
-  // One unit per CTA when there are no more units than CTAs; else the
-  // group-aligned split when it gives no CTA more units than the contiguous
-  // one (with several units a CTA, mostly at small m, a CTA that straddles two
-  // groups would stage and split a second weight group on its critical path).
+  // One unit per CTA when there are no more units than CTAs.  Else the
+  // group-aligned split on floor(ctas / groups) CTAs per group, when its
+  // largest share is within 10 % of the contiguous split's: no CTA then
+  // stages and splits a second weight group on its critical path, and the
+  // CTAs of all groups sweep the same token tiles together, so that the
+  // tokens' rows are read from HBM close together in time.
   const int tiles = (p.m + UT - 1) / UT, units = tiles * p.slices;
-  const int grid = units < ctas ? units : ctas;
+  int grid = units < ctas ? units : ctas;
   StageParams q = p;
   q.group_aligned = 0;
   if (units > ctas && ctas >= p.slices && p.fn_terms > 0) {
-    const int per = ctas / p.slices;   // fewest CTAs any group gets
-    q.group_aligned = (tiles + per - 1) / per <= (units + ctas - 1) / ctas;
+    const int per = ctas / p.slices;
+    if (10 * ((tiles + per - 1) / per) <= 11 * ((units + ctas - 1) / ctas)) {
+      q.group_aligned = 1;
+      grid = per * p.slices;
+    }
   }
   const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
   // programmatic dependent launch: the CTAs' setup (and, for a layer weight,
