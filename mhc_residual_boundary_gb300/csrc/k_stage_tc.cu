@@ -2,9 +2,11 @@
 // cores, prenorm GEMV on tcgen05 tensor cores.
 //
 // Work unit: 32 tokens x one group of 128 hidden columns (every row piece a
-// unit reads is a 256-byte run).  Units are numbered group-major and every
-// CTA (one per SM, persistent) takes a contiguous range of them, so a CTA
-// stages each group's hc_fn once.  Roles in a CTA of 18 warps:
+// unit reads is a 256-byte run).  Units are numbered group-major.  Each CTA
+// (persistent, one per SM) takes a contiguous range of them, or, when that
+// costs no more than 10 % in its largest share, the CTAs are shared out over
+// the groups and each takes a contiguous range of its group's token tiles
+// (the launcher decides).  Roles in a CTA of 18 warps:
 //
 //   producer warp (one lane issues): refills ring slots as soon as the mixer
 //     warps release them -- stage q (tokens 8q .. 8q+7) of every unit by four
@@ -13,14 +15,17 @@
 //     comb [m][4][4], counted on the slot's mbarrier; out-of-range tokens and
 //     columns arrive as zeros.
 //   MMA warp (one lane issues): a unit's MMAs as soon as its A operand is
-//     complete; it also owns the tensor memory.
+//     complete, then the unit's new streams from A to residual_out by two
+//     swizzled TMA tensor stores; it releases A (the MMA barrier) once the
+//     MMAs are done and the stores have read A.  It also owns the tensor
+//     memory.
 //   16 mixer warps: four per stage, one (token, 16-byte fragment) item per
 //     thread.  Stage-1 sum of the tp partials in FP32 in rank order, rounded
 //     to BF16 ([DSV] _LamportMHCDeviceKernel.kernel, lane_sum); post-mix of
-//     the four streams ([GLM] _BoundaryDeviceKernel.kernel, "mixed"), stored
-//     to residual_out and, as the MMA's A operand, to shared memory; the sum
-//     of squares of the new streams over the token's 16 lanes.  They also
-//     build the B operand when the group changes and read the accumulators.
+//     the four streams ([GLM] _BoundaryDeviceKernel.kernel, "mixed"), written
+//     as the MMA's A operand to shared memory; the sum of squares of the new
+//     streams over the token's 16 lanes.  They also build the B operand when
+//     the group changes and read the accumulators.
 //   GEMV (tensor cores): the MMA's 128 rows are (token t, stream j) with
 //     row = 4t + j, its K the unit's 128 columns and its 96 columns (stream
 //     j', output i): D[(t,j)][(j',i)] = sum_h new_j[t][h] * fn[j'*H + h][i];
@@ -29,11 +34,12 @@
 //     split into three BF16 terms (hi + mid + lo, remainder below 2^-24
 //     relative) so that each BF16 x BF16 product is exact and the sum
 //     accumulates in FP32 in tensor memory: 3 x 8 MMAs of M=128, N=96, K=16
-//     into one of two accumulators (by unit parity).
+//     into one of two accumulators (by unit parity).  A BF16 weight ([GLM]
+//     `fn`, [24][4H]) is one term: 8 MMAs.
 //   order of a mixer iteration: post-mix of unit i, wait for unit i - 1's
-//     MMAs, A rows of unit i to shared memory and to the MMA warp, then --
-//     while those MMAs run -- the global stores of unit i and the epilogue
-//     of unit i - 1.
+//     MMAs (and stores), A rows of unit i to shared memory and to the MMA
+//     warp, then -- while those MMAs run -- the token sums of squares and the
+//     epilogue of unit i - 1.
 //   epilogue (one unit later):
 //     warp w reads TMEM lane quarter w % 4 (the rows of stage w % 4's
 //     tokens, four lanes per token) and six of the 24 outputs of all four
@@ -42,11 +48,15 @@
 //     sums go to the scratch rows [m][groups][25] (24 sums + the sum of
 //     squares; rows padded to 16 bytes) that the finish kernel reduces.
 //
-// A group's hc_fn rows (FP32) arrive by four bulk copies into the A buffer,
-// which is idle at that point, and the mixers split them into B from shared
-// memory; the producer issues the first group's copies before anything else
-// and prefetches the later groups' rows into L2.  Every wait is bounded; a wait that gives up sets bit 1 of the error
-// word and stops the CTA.
+// A group's weight rows arrive by bulk (FP32) or tiled (BF16) copies into
+// the A buffer, which is idle at that point, and the mixers split or place
+// them into B from shared memory.  The kernel is a programmatic dependent
+// launch: set-up, and for a layer weight the first group's staging and
+// split, happen before it waits for the preceding kernel; the producer
+// prefetches the later groups' rows into L2.  Without the GEMV (the
+// delayed-mHC consumer) there is no A, B or MMA, and the mixers store the
+// new streams themselves.  Every wait is bounded; a wait that gives up sets
+// bit 1 of the error word and stops the CTA.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.

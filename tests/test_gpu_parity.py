@@ -87,6 +87,15 @@ def test_bf16_weight(Boundary, hidden, tp, m, mxfp8):
     check(Boundary, hidden, tp, m, mxfp8=mxfp8, bf16_weight=True, seed=7 * m + hidden)
 
 
+@pytest.mark.parametrize("hidden,tp,m,bf16", [(1032, 4, 3, False), (1032, 4, 5, True), (16384, 8, 8, False),
+                                              (16384, 2, 8, True), (6144, 8, 8, False), (6144, 8, 9, False),
+                                              (8, 1, 8, False), (136, 3, 7, True)])
+def test_few_tokens(Boundary, hidden, tp, m, bf16):
+    # up to 8 tokens, one unit a CTA: ragged last groups, both weight forms,
+    # the largest width, one and nine tokens around a stage's eight
+    check(Boundary, hidden, tp, m, bf16_weight=bf16, mxfp8=hidden % 128 == 0, seed=hidden + 3 * m)
+
+
 @pytest.mark.parametrize("hidden,tp,m,bf16", [(2048, 6, 1024, False), (2048, 3, 1024, False),
                                               (6144, 8, 512, True), (2048, 8, 1024, True)])
 def test_ring_wraps_many_times(Boundary, hidden, tp, m, bf16):
