@@ -12,10 +12,11 @@
 // An index outside [-1, rows) sets bit 0 of the error word and is treated as
 // a route not held.
 //
-// Layout: one CTA of 128 threads per (token, 1024-column chunk), grid-stride;
-// the token's indices and weights are staged in shared memory, and each
-// thread takes one 16-byte fragment, loading eight routes' fragments before
-// the multiply-adds so that eight loads are in flight per thread.
+// Layout: CTAs of 8 warps, grid-stride over (token, 256-column chunk) jobs.
+// Lane l of every warp takes the chunk's 16-byte fragment l, so that a warp
+// reads 512 contiguous bytes of a route row; warp w folds ranks w, w + 8, ...,
+// loading all of a rank's routes (eight at a time) before the multiply-adds.
+// The folded x_r go to shared memory, and warp 0 adds them in rank order.
 //
 // Page: [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
 #include "device_common.cuh"
@@ -24,82 +25,88 @@
 namespace mhc {
 namespace {
 
-constexpr int NT = 128;
+constexpr int WARPS = 8;
+constexpr int NT = WARPS * 32;
 constexpr int KB = 8;                        // routes loaded per batch
-constexpr int MAX_ROUTES = 32 * 64;          // tp * top_k the shared staging holds
+constexpr int TP_MAX = 32;
 
 __global__ void __launch_bounds__(NT) k_moe_fold(const FoldParams p) {
-  __shared__ int idx_s[MAX_ROUTES];
-  __shared__ float w_s[64];
-  const int H = p.hidden, K = p.top_k, routes = p.tp * p.top_k;
-  const int nfrag = H / VEC, chunks = (nfrag + NT - 1) / NT;
+  extern __shared__ float4 xs[];             // [tp][32][2]: x_r of the chunk's 32 fragments
+  const int H = p.hidden, K = p.top_k, nfrag = H / VEC;
+  const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
+  const int chunks = (nfrag + 31) / 32;
   for (int job = blockIdx.x; job < p.m * chunks; job += gridDim.x) {
-    const int t = job / chunks, fr = (job % chunks) * NT + threadIdx.x;
-    __syncthreads();   // the previous token's routes are no longer read
-    for (int e = threadIdx.x; e < routes; e += NT) {
-      const int r = e / K, k = e % K;
-      int row = p.idx[((size_t)r * p.m + t) * K + k];
-      if (row < -1 || row >= p.rows_per_rank) {
-        atomicOr(p.err, 1u);
-        row = -1;
+    const int t = job / chunks, fr = (job % chunks) * 32 + lane;
+    const bool live = fr < nfrag;
+#pragma unroll 1
+    for (int r = warp; r < p.tp; r += WARPS) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      if (live) {
+        const int32_t *ix = p.idx + ((size_t)r * p.m + t) * K;
+        const float *wt = p.weights + (size_t)t * K;
+        const uint16_t *rows = p.routed + (size_t)r * p.rows_per_rank * H + (size_t)fr * VEC;
+#pragma unroll 1
+        for (int k0 = 0; k0 < K; k0 += KB) {
+          int row[KB];
+          uint4 v[KB];
+#pragma unroll
+          for (int i = 0; i < KB; ++i) {
+            row[i] = k0 + i < K ? ix[k0 + i] : -1;
+            if (row[i] < -1 || row[i] >= p.rows_per_rank) {
+              atomicOr(p.err, 1u);
+              row[i] = -1;
+            }
+            v[i] = row[i] >= 0 ? ld_stream(rows + (size_t)row[i] * H) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int i = 0; i < KB; ++i) {
+            if (row[i] >= 0) {
+              float a[8];
+              unpack8(v[i], a);
+              const float w = wt[k0 + i];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] = __fmaf_rn(a[e], w, x[e]);
+            }
+          }
+        }
+        float s[8];
+        unpack8(ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)fr * VEC), s);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(x[e], s[e]);
+        round8(x);
       }
-      idx_s[e] = row;
+      xs[(r * 32 + lane) * 2] = make_float4(x[0], x[1], x[2], x[3]);
+      xs[(r * 32 + lane) * 2 + 1] = make_float4(x[4], x[5], x[6], x[7]);
     }
-    for (int k = threadIdx.x; k < K; k += NT) w_s[k] = p.weights[(size_t)t * K + k];
     __syncthreads();
-    if (fr < nfrag) {
-      const size_t h = size_t(fr) * VEC;
+    if (warp == 0 && live) {
+      // y = bf16(((0 + x_0) + x_1) + ...)
       float y[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = 0.f;
 #pragma unroll 1
       for (int r = 0; r < p.tp; ++r) {
-        const uint16_t *rows_r = p.routed + (size_t)r * p.rows_per_rank * H + h;
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 1
-        for (int k0 = 0; k0 < K; k0 += KB) {
-          uint4 x[KB];
-#pragma unroll
-          for (int i = 0; i < KB; ++i) {
-            const int k = k0 + i;
-            const int row = k < K ? idx_s[r * K + k] : -1;
-            x[i] = row >= 0 ? ld_stream(rows_r + (size_t)row * H) : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int i = 0; i < KB; ++i) {
-            const int k = k0 + i;
-            if (k < K && idx_s[r * K + k] >= 0) {
-              float v[8];
-              unpack8(x[i], v);
-              const float w = w_s[k];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(v[e], w, acc[e]);
-            }
-          }
-        }
-        float s[8];
-        unpack8(ld_stream(p.shared + ((size_t)r * p.m + t) * H + h), s);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], s[e]);
-        round8(acc);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], acc[e]);
+        const float4 a = xs[(r * 32 + lane) * 2], b = xs[(r * 32 + lane) * 2 + 1];
+        y[0] = __fadd_rn(y[0], a.x); y[1] = __fadd_rn(y[1], a.y);
+        y[2] = __fadd_rn(y[2], a.z); y[3] = __fadd_rn(y[3], a.w);
+        y[4] = __fadd_rn(y[4], b.x); y[5] = __fadd_rn(y[5], b.y);
+        y[6] = __fadd_rn(y[6], b.z); y[7] = __fadd_rn(y[7], b.w);
       }
-      st_vec(p.y + (size_t)t * H + h, round8(y));
+      st_vec(p.y + (size_t)t * H + (size_t)fr * VEC, round8(y));
     }
+    __syncthreads();   // the next job's x_r overwrite these
   }
 }
 
 }  // namespace
 
 cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream) {
-  if (p.tp < 1 || p.top_k < 1 || p.top_k > 64 || p.tp * p.top_k > MAX_ROUTES || p.hidden % VEC)
-    return cudaErrorInvalidValue;
-  const int jobs = p.m * ((p.hidden / VEC + NT - 1) / NT);
+  if (p.tp < 1 || p.tp > TP_MAX || p.top_k < 1 || p.top_k > 64 || p.hidden % VEC) return cudaErrorInvalidValue;
+  const int jobs = p.m * ((p.hidden / VEC + 31) / 32);
   const int grid = jobs < ctas ? jobs : ctas;
-  k_moe_fold<<<grid, NT, 0, stream>>>(p);
+  k_moe_fold<<<grid, NT, size_t(p.tp) * 32 * 2 * sizeof(float4), stream>>>(p);
   return cudaGetLastError();
 }
 

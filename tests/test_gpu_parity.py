@@ -64,6 +64,14 @@ def test_moe_routes_not_held(Boundary, tp, k, holes, m):
     check(Boundary, 512, tp, m, moe=True, top_k=k, holes=holes, seed=tp * 10 + k)
 
 
+@pytest.mark.parametrize("hidden,tp,k,holes,m", [(256, 32, 3, 0.2, 9), (520, 5, 13, 0.3, 21), (128, 2, 64, 0.5, 4),
+                                                 (1032, 16, 9, 0.1, 3)])
+def test_moe_fold_shapes(Boundary, hidden, tp, k, holes, m):
+    # the fold's lane groups: a full warp of ranks, ranks padded to a power of
+    # two, more than one batch of routes, a ragged last chunk of columns
+    check(Boundary, hidden, tp, m, moe=True, top_k=k, holes=holes, seed=hidden + tp + k)
+
+
 def test_large_mxfp8(Boundary):
     rep = check(Boundary, 6144, 8, 4096, mxfp8=True, seed=4)
     print("large_mxfp8 report:", rep)
