@@ -122,7 +122,8 @@ struct Layout {
   static constexpr int afull = empty + 8 * MAX_SLOTS;   // uint64: A operand complete
   static constexpr int mma = afull + 8;                 // uint64 [2]: MMAs of a unit done
   static constexpr int bfull = mma + 16;                // uint64: a group's hc_fn rows staged
-  static constexpr int slot = bfull + 8;                // TMEM address
+  static constexpr int bbuilt = bfull + 8;              // uint64: every mixer warp has split a group into B
+  static constexpr int slot = bbuilt + 8;               // TMEM address
   static constexpr int abort = slot + 4;                // int
   static constexpr int b = 1024;
   static_assert(abort + 4 <= b, "control block");
@@ -271,6 +272,16 @@ __device__ __forceinline__ void build_b(const StageParams &p, int g, const unsig
     place_b_bf16(stg, group_rows(p.hidden, g), b_s);
 }
 
+// The mixer warps' barrier after splitting weight group number `loads`
+// (1, 2, ...): each warp arrives once, then waits, with a bound, for the
+// phase of that group; a barrier with a bounded wait, so that a warp that has
+// left the loop after a failed wait cannot hold the others forever.
+__device__ __forceinline__ bool b_built(uint64_t *bbuilt, int loads, int lane) {
+  __syncwarp();
+  if (lane == 0) tc::mbar_arrive(bbuilt);
+  return tc::mbar_wait_bounded(bbuilt, uint32_t((loads - 1) & 1), WAIT_LIMIT);
+}
+
 // ------------------------------------------------------------- epilogue
 // Unit `i`'s GEMV sums once its MMAs are done.  Warp w reads lane quarter
 // w % 4 -- row 32q + l = (token 8q + l/4, stream l%4) -- and outputs
@@ -399,6 +410,7 @@ __global__ void __launch_bounds__(NT, 1)
   uint64_t *afull = reinterpret_cast<uint64_t *>(smem + Layout::afull);
   uint64_t *mma_bar = reinterpret_cast<uint64_t *>(smem + Layout::mma);
   uint64_t *bfull = reinterpret_cast<uint64_t *>(smem + Layout::bfull);
+  uint64_t *bbuilt = reinterpret_cast<uint64_t *>(smem + Layout::bbuilt);
   uint32_t *slot = reinterpret_cast<uint32_t *>(smem + Layout::slot);
   volatile int *abort_s = reinterpret_cast<volatile int *>(smem + Layout::abort);
   unsigned char *a_s = smem + layout_a(p.fn_terms);
@@ -461,6 +473,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::mbar_init(&mma_bar[0], 1);
       tc::mbar_init(&mma_bar[1], 1);
       tc::mbar_init(bfull, 1);
+      tc::mbar_init(bbuilt, MIX_WARPS);
       *abort_s = 0;
       tc::mbar_init_fence();
       tc::tma_prefetch_desc(&tm_part);
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(NT, 1)
       ++loads;
       build_b(p, first_group, a_s, b_s);
       // every mixer has read the staged rows before any A row is written
-      asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
+      if (!b_built(bbuilt, loads, lane)) *abort_s = 1;
       cur_group = first_group;
     }
     pdl_wait();
@@ -615,7 +628,10 @@ __global__ void __launch_bounds__(NT, 1)
         ++loads;
         build_b(p, g, a_s, b_s);
         // every mixer has read the staged rows before any A row is written
-        asm volatile("bar.sync 1, %0;" ::"n"(MIX_THREADS) : "memory");
+        if (!b_built(bbuilt, loads, lane)) {
+          *abort_s = 1;
+          break;
+        }
         cur_group = g;
       }
 #pragma unroll
