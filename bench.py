@@ -65,7 +65,7 @@ def workload(name, m):
     if w is None:
         base = cands[-1]
         w = synth.Workload(base.name, base.hidden, base.tp, m, base.top_k, base.moe, base.mxfp8, base.bf16_fn,
-                           base.consume, base.residual_only)
+                           base.consume, base.residual_only, base.owner)
     return w
 
 
@@ -77,6 +77,8 @@ def call_bytes(w):
         stage1 = tp * K * 2 * H + tp * 2 * H + tp * K * 4 + K * 4
     else:
         stage1 = 2 * tp * H
+    if w.owner:
+        stage1 += 4 * H   # the owners' sums, written and read back
     if w.consume:
         # the delayed-mHC consumer: no weight, no mixes; pre read, layer input written
         stage = M * (stage1 + 8 * H + 8 * H + 16 + 64)
@@ -102,6 +104,7 @@ def describe(w):
             "weight": "none (carried pre)" if w.consume else "bf16 [24][4H]" if w.bf16_fn else "f32 [4H][24]",
             "weight_staging": ("layer weight: staged while the preceding kernel ends" if STATIC_WEIGHT
                                else "after the preceding kernel"),
+            "reduction": "MoE fold" if w.moe else "two-shot (owner reduce)" if w.owner else "direct",
             "residual_only": w.residual_only}
 
 
@@ -295,7 +298,7 @@ def run_ours(args, w):
 
     dev_in = {("norm_weight" if k == "gamma" else k): to_dev(v) for k, v in inputs.items()}
     b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
-                 host_staging=not w.moe, static_weight=STATIC_WEIGHT, device=local)
+                 host_staging=not w.moe, static_weight=STATIC_WEIGHT, owner_reduce=w.owner, device=local)
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
     nbytes = call_bytes(w)
@@ -429,7 +432,7 @@ def run_sweep(args):
                       (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
                        else torch.from_numpy(v)).to(device) for k, v in inputs.items()}
             b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
-                         static_weight=STATIC_WEIGHT)
+                         static_weight=STATIC_WEIGHT, owner_reduce=w.owner)
             nbytes = call_bytes(w)
             nsets = 1 if nbytes["total"] >= 3 * l2 else math.ceil(3 * l2 / nbytes["total"]) + 1
             def outputs():

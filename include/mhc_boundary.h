@@ -92,7 +92,16 @@ enum {
    * into tensor-core operands then, ahead of the wait for that kernel.  The
    * partials, streams, post and comb are read only after the wait in any
    * case.  Results are the same bits with or without the flag. */
-  MHC_FLAG_STATIC_WEIGHT = 1u << 4
+  MHC_FLAG_STATIC_WEIGHT = 1u << 4,
+  /* [DSV] two-shot (BT) reduction, emulated on one GPU: an owner-reduce
+   * kernel first sums the tp partials of every token (token t's owner is
+   * rank t % tp) in FP32 from rank 0 and rounds to BF16, into a library
+   * buffer of max_num_tokens x H BF16 allocated in create; the boundary then
+   * takes those sums as its one partial.  Same bits as the direct sum; one
+   * more kernel and 4H more bytes a token.  Applies to mhc_boundary_run and
+   * to mhc_boundary_consume with partials; a MoE call folds its routes
+   * instead. */
+  MHC_FLAG_OWNER_REDUCE = 1u << 5
 };
 
 /* Construction arguments ([GLM] AllReduceMhcBoundary.__init__, [DSV]
@@ -317,7 +326,8 @@ mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *config, const 
  * tools; off by default). */
 typedef struct {
   int32_t calls;    /* calls recorded */
-  float stage_ms;   /* stage kernel: stage 1 / MoE fold, post-mix, partial GEMV */
+  float stage_ms;   /* stage kernel (with the MoE fold or owner reduce before it):
+                       stage 1, post-mix, partial GEMV */
   float finish_ms;  /* finish kernel: pre, collapse, RMSNorm, MXFP8 */
   float mixes_ms;   /* side kernel: post and Sinkhorn */
 } mhc_profile_t;
@@ -330,8 +340,9 @@ mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls);
 mhc_status_t mhc_boundary_profile_end(mhc_boundary_t *b, mhc_profile_t *out);
 
 /* Kernels one mhc_boundary_run call launches: stage + finish, plus the
- * post / Sinkhorn kernel with MHC_FLAG_SIDE_MIXES or MHC_FLAG_SYNC_MIXES.
- * mhc_boundary_finalize_moe launches one more (the MoE fold). */
+ * post / Sinkhorn kernel with MHC_FLAG_SIDE_MIXES or MHC_FLAG_SYNC_MIXES, plus
+ * the owner reduce with MHC_FLAG_OWNER_REDUCE.  mhc_boundary_finalize_moe
+ * launches the MoE fold in its place, or one more kernel without that flag. */
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b);
 
 const char *mhc_status_string(mhc_status_t status);

@@ -58,7 +58,7 @@ class Boundary:
                  top_k: int = 0, rms_eps: float = 1e-6, hc_eps: float = 1e-6,
                  post_mult: float = 2.0, norm_eps: float = 1e-6, mxfp8: bool = False,
                  sync_mixes: bool = False, side_mixes: bool = False, host_staging: bool = False,
-                 static_weight: bool = False, device=None):
+                 static_weight: bool = False, owner_reduce: bool = False, device=None):
         if device is None:
             device = torch.cuda.current_device()
         self.device = torch.device("cuda", int(torch.device("cuda", device).index
@@ -66,7 +66,8 @@ class Boundary:
         flags = ((capi.MHC_FLAG_MXFP8 if mxfp8 else 0) | (capi.MHC_FLAG_SYNC_MIXES if sync_mixes else 0)
                  | (capi.MHC_FLAG_HOST_STAGING if host_staging else 0)
                  | (capi.MHC_FLAG_SIDE_MIXES if side_mixes else 0)
-                 | (capi.MHC_FLAG_STATIC_WEIGHT if static_weight else 0))
+                 | (capi.MHC_FLAG_STATIC_WEIGHT if static_weight else 0)
+                 | (capi.MHC_FLAG_OWNER_REDUCE if owner_reduce else 0))
         self.config = capi.mhc_boundary_config_t(hidden, HC, tp, max_num_tokens, sinkhorn_repeat, top_k,
                                                  rms_eps, hc_eps, post_mult, norm_eps, flags)
         self.hidden, self.tp, self.top_k, self.capacity = hidden, tp, top_k, max_num_tokens

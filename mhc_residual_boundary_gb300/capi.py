@@ -22,6 +22,7 @@ MHC_FLAG_SYNC_MIXES = 1 << 1
 MHC_FLAG_HOST_STAGING = 1 << 2
 MHC_FLAG_SIDE_MIXES = 1 << 3
 MHC_FLAG_STATIC_WEIGHT = 1 << 4
+MHC_FLAG_OWNER_REDUCE = 1 << 5
 
 
 class MhcError(RuntimeError):

@@ -39,7 +39,7 @@ struct mhc_boundary {
   unsigned long long side_capture = 0;
   float *mixes = nullptr;        // [cap][24] raw mixes read by the side kernel
   float *part = nullptr;         // [cap][part_row_floats(slices)] stage-kernel partial sums
-  uint16_t *fold = nullptr;      // [cap][H] bf16 stage-1 sum of MoE calls (top_k > 0)
+  uint16_t *fold = nullptr;      // [cap][H] bf16 stage-1 sum of MoE calls (top_k > 0) or owner sums
   unsigned int *err = nullptr;   // device-detected argument errors
   unsigned char *staging = nullptr;
   size_t staging_bytes = 0;
@@ -245,6 +245,14 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
+  } else if (c.flags & MHC_FLAG_OWNER_REDUCE) {
+    // two-shot reduction: the owners' sums, then the stage kernel takes
+    // them as its single partial
+    const OwnerParams op = {a->m, c.hidden, c.tp, static_cast<const uint16_t *>(a->partials), b->fold};
+    e = launch_owner_reduce(op, b->sm_count * 16, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "owner reduce kernel: %s", cudaGetErrorString(e));
+    sp.tp = 1;
+    sp.partials = b->fold;
   }
   // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
   // groups (tensor-core kernel); the scratch holds the larger count
@@ -367,6 +375,12 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
+  } else if (c.flags & MHC_FLAG_OWNER_REDUCE) {
+    const OwnerParams op = {a->m, c.hidden, c.tp, static_cast<const uint16_t *>(a->partials), b->fold};
+    e = launch_owner_reduce(op, b->sm_count * 16, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "owner reduce kernel: %s", cudaGetErrorString(e));
+    sp.tp = 1;
+    sp.partials = b->fold;
   }
   sp.slices = (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS;
   sp.residual = static_cast<const uint16_t *>(a->residual);
@@ -481,7 +495,7 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
   if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_HOST_STAGING | MHC_FLAG_SIDE_MIXES |
-                          MHC_FLAG_STATIC_WEIGHT))
+                          MHC_FLAG_STATIC_WEIGHT | MHC_FLAG_OWNER_REDUCE))
     return fail(g_create_error, MHC_ERR_INVALID_ARG, "unknown flag bits 0x%x", c.flags);
   int count = 0;
   if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count)
@@ -508,7 +522,8 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   }
   e = cudaMalloc(&b->mixes, cap * MIX * sizeof(float));
   if (e == cudaSuccess) e = cudaMalloc(&b->part, cap * part_row_floats(b->slices) * sizeof(float));
-  if (e == cudaSuccess && c.top_k > 0) e = cudaMalloc(&b->fold, cap * size_t(c.hidden) * 2);
+  if (e == cudaSuccess && (c.top_k > 0 || (c.flags & MHC_FLAG_OWNER_REDUCE)))
+    e = cudaMalloc(&b->fold, cap * size_t(c.hidden) * 2);
   if (e == cudaSuccess) e = cudaMalloc(&b->err, sizeof(unsigned int));
   if (e == cudaSuccess) e = cudaMemset(b->err, 0, sizeof(unsigned int));
   if (e == cudaSuccess && (c.flags & MHC_FLAG_HOST_STAGING)) {
@@ -680,7 +695,8 @@ size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden) { return scale_bytes(m, 
 
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) {
   if (!b) return 0;
-  return (b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 3 : 2;
+  return ((b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 3 : 2) +
+         ((b->cfg.flags & MHC_FLAG_OWNER_REDUCE) ? 1 : 0);
 }
 
 mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls) {

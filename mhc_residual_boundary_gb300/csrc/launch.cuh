@@ -80,6 +80,14 @@ struct FinishParams {
   unsigned int *err;          // device error word (bit 1: a wait gave up) or null
 };
 
+// Two-shot reduction (single-GPU emulation of the owner reduce): the tp
+// partials [tp][m][H] summed per token into sums [m][H].
+struct OwnerParams {
+  int m, hidden, tp;
+  const uint16_t *partials;   // [tp][m][H]
+  uint16_t *sums;             // [m][H]
+};
+
 // MoE fold: stage 1 of a MoE-finalize call into a [m][H] BF16 buffer.
 struct FoldParams {
   int m, hidden, tp, top_k, rows_per_rank;
@@ -119,5 +127,6 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
 // MoE fold over at most `ctas` CTAs of 128 threads.
 cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream);
+cudaError_t launch_owner_reduce(const OwnerParams &p, int ctas, cudaStream_t stream);
 
 }  // namespace mhc

@@ -49,6 +49,7 @@ class Workload:
     bf16_fn: bool = False    # prenorm weight as BF16 [24][4H] instead of FP32 [4H][24]
     consume: bool = False    # the delayed-mHC consumer: carried pre, no GEMV
     residual_only: bool = False
+    owner: bool = False      # two-shot reduction: an owner reduce sums the partials first
 
 
 # The workloads this boundary is measured and checked on.
@@ -64,6 +65,9 @@ WORKLOADS = {
     # the delayed-mHC consumer (carried pre) and its residual-only form
     "consume": [Workload("consume", 6144, 8, m, consume=True) for m in (1, 256, 4096)],
     "residual_only": [Workload("residual_only", 6144, 8, 4096, consume=True, residual_only=True)],
+    # the two-shot (owner-reduce) reduction emulated on one GPU
+    "owner_reduce": [Workload("owner_reduce", 6144, 4, 256, owner=True),
+                     Workload("owner_reduce", 6144, 8, 4096, mxfp8=True, owner=True)],
 }
 
 

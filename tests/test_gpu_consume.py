@@ -23,12 +23,12 @@ def Boundary():
 
 
 def run_consume(Boundary, hidden, tp, m, *, seed, moe=False, top_k=0, holes=0.0, mxfp8=False,
-                residual_only=False):
+                residual_only=False, owner_reduce=False):
     inp = synth.make_inputs(hidden, tp, m, top_k=top_k, moe=moe, seed=seed, holes=holes)
     pre = np.random.default_rng(seed).uniform(0.05, 1.2, (m, HC)).astype(np.float32)
     p = oracle.Problem(hidden, tp, m, top_k=top_k, rows_per_rank=m * top_k if moe else 0)
     ref = oracle.consume(p, inp, pre, moe=moe, mxfp8_out=mxfp8, residual_only=residual_only)
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, top_k=top_k, mxfp8=mxfp8)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m, top_k=top_k, mxfp8=mxfp8, owner_reduce=owner_reduce)
     try:
         dev = to_device(inp)
         if moe:
