@@ -388,9 +388,12 @@ def run_ours(args, w):
         oracle.build()
         threads = os.cpu_count() or 1
         sample = w.m
+        one = min(sample, 512)
         cpu = {"value": oracle_tokens_per_s(w, inputs, sample, threads), "unit": "tokens/s",
                "cores": threads, "kind": "oracle",
-               "sample": f"all {sample} tokens of the workload once, token ranges over {threads} threads"}
+               "sample": f"all {sample} tokens of the workload once, token ranges over {threads} threads",
+               "single_thread_value": oracle_tokens_per_s(w, inputs, one, 1),
+               "single_thread_sample": f"the first {one} tokens on one thread"}
 
     launches = b.launches_per_call() + (1 if w.moe else 0)
     b.close()
@@ -487,6 +490,28 @@ def run_sweep(args):
                 torch.cuda.synchronize()
                 graph_us = start.elapsed_time(stop) * 1e3 / (reps * nsets)
                 del g
+            # hot L2 (labelled as such): the same graph replay on one buffer
+            # set, so that a workload smaller than L2 reads it from L2
+            hot_us = None
+            if nsets > 1:
+                cap = torch.cuda.Stream()
+                cap.wait_stream(stream)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    for _ in range(16):
+                        call(*sets[0], stream=cap)
+                    b.join(cap)
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                reps = max(1, steps // 16)
+                start.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                stop.record(stream)
+                torch.cuda.synchronize()
+                hot_us = start.elapsed_time(stop) * 1e3 / (reps * 16)
+                del g
             b.check_errors()
             b.close()
             n = max(prof["calls"], 1)
@@ -497,6 +522,7 @@ def run_sweep(args):
                 "frac_8tbs": gbs / 8000.0, "buffer_sets": nsets, "steps": steps,
                 "graph_us_per_call": graph_us,
                 "graph_gbs": nbytes["total"] / (graph_us * 1e-6) / 1e9 if graph_us else None,
+                "hot_l2_graph_us_per_call": hot_us,
                 "kernel_us": {"stage": prof["stage_ms"] / n * 1e3, "finish": prof["finish_ms"] / n * 1e3,
                               "mixes": prof["mixes_ms"] / n * 1e3},
             }), flush=True)
