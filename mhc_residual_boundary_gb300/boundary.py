@@ -52,7 +52,15 @@ REQUIRED_OUTPUTS = ("residual_out", "layer_input", "post_out", "comb_out")
 class Boundary:
     """One boundary instance: it serves every call of up to max_num_tokens
     tokens ([GLM] AllReduceMhcBoundary: one instance serves every boundary
-    of the model, one after another)."""
+    of the model, one after another).
+
+    Flags (include/mhc_boundary.h): mxfp8 (accept the MXFP8 outputs),
+    sync_mixes / side_mixes (post and Sinkhorn in a separate kernel on the
+    caller's stream / a side stream), host_staging (allow run_host),
+    static_weight (the prenorm weight is a layer weight, staged while the
+    kernel before the call finishes), owner_reduce (the two-shot reduction:
+    an owner-reduce kernel sums the partials first).  All give the same
+    results."""
 
     def __init__(self, *, hidden: int, tp: int, max_num_tokens: int, sinkhorn_repeat: int = 20,
                  top_k: int = 0, rms_eps: float = 1e-6, hc_eps: float = 1e-6,

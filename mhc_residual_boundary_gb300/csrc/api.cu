@@ -1,9 +1,12 @@
 // api.cu -- host implementation of include/mhc_boundary.h.
 //
 // Call structure ([GLM] AllReduceMhcBoundary.__call__ / join): on the
-// caller's stream, the MoE fold kernel (finalize_moe only), the stage kernel
-// and the finish kernel (programmatic dependent launch), which also computes
-// post and the Sinkhorn mix.  With MHC_FLAG_SIDE_MIXES the post / Sinkhorn
+// caller's stream, the MoE fold kernel (finalize_moe) or the owner-reduce
+// kernel (MHC_FLAG_OWNER_REDUCE), then the stage kernel and the finish
+// kernel, both programmatic dependent launches; the finish kernel also
+// computes post and the Sinkhorn mix.  With MHC_FLAG_STATIC_WEIGHT the stage
+// kernel stages and splits the prenorm weight before it waits for the
+// kernel ahead of it.  With MHC_FLAG_SIDE_MIXES the post / Sinkhorn
 // kernel runs instead on a library side stream after an event; the next call
 // (or join) waits for its completion event.  With MHC_FLAG_SYNC_MIXES that
 // kernel runs on the caller's stream.  Every argument is validated before the
