@@ -117,8 +117,8 @@ static_assert(UK % 16 == 0 && UN % 16 == 0 && UN <= 256, "MMA shape");
 // for a BF16 weight), A (whose space also takes a group's staged weight
 // rows), then the ring of stage slots.
 struct Layout {
-  static constexpr int full = 0;                        // uint64 [MAX_SLOTS]
-  static constexpr int empty = full + 8 * MAX_SLOTS;    // uint64 [MAX_SLOTS]
+  static constexpr int full = 0;                        // uint64 [MAX_SLOTS][2] (see full_bar)
+  static constexpr int empty = full + 16 * MAX_SLOTS;   // uint64 [MAX_SLOTS]
   static constexpr int afull = empty + 8 * MAX_SLOTS;   // uint64: A operand complete
   static constexpr int mma = afull + 8;                 // uint64 [2]: MMAs of a unit done
   static constexpr int bfull = mma + 16;                // uint64: a group's hc_fn rows staged
@@ -145,19 +145,32 @@ __host__ __device__ constexpr int slot_res(int tp) { return tp * QT * ROW; }
 __host__ __device__ constexpr int slot_post(int tp) { return slot_res(tp) + QT * HC * ROW; }
 __host__ __device__ constexpr int slot_comb(int tp) { return slot_post(tp) + QT * HC * 4; }
 __host__ __device__ constexpr int slot_bytes(int tp) { return slot_comb(tp) + QT * HC * HC * 4; }
-// Ring slots: a multiple of the four stages of a unit, so that slot
-// n % nslot always serves stage n % 4 and every use of a slot is consumed by
-// the same four warps in order.  (With, say, six slots a slot would alternate
-// between two stages' warps, and a warp waiting for the slot's use two ahead
-// could pass on the parity of the use before it.)
+// Ring slots: 8, 6 or 4 (as many as the shared memory holds).  Slot n % nslot
+// takes stage n % 4.  With 4 or 8 slots every use of a slot is consumed by
+// the same four warps in order.  With 6 a slot alternates between two
+// stages' warps; an mbarrier tells phases apart only by parity, so each slot
+// then has two "full" barriers, one for its even and one for its odd uses,
+// each consumed by one stage's warps in order (full_bar).
 __host__ __device__ constexpr int ring_slots(int tp, int terms) {
-  return ((SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) < MAX_SLOTS
-              ? (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp)
-              : MAX_SLOTS) / NSTAGE * NSTAGE;
+  return (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) >= 8   ? 8
+         : (SMEM_MAX - layout_ring(terms)) / slot_bytes(tp) >= 6 ? 6
+                                                                 : 4;
 }
 static_assert(slot_bytes(1) % 128 == 0 && slot_post(1) % 128 == 0 && slot_comb(1) % 128 == 0, "slot alignment");
 static_assert(ring_slots(TP_TMA_MAX, 3) >= NSTAGE, "a unit's four stages fit the ring");
-static_assert(MAX_SLOTS % NSTAGE == 0, "slot n % nslot serves stage n % 4");
+static_assert(MAX_SLOTS == 8 && (SMEM_MAX - layout_ring(3)) / slot_bytes(TP_TMA_MAX) >= 4, "ring of 4, 6 or 8 slots");
+
+// The "full" barrier of fill n (slot n % nslot, use n / nslot) and the parity
+// of that use's phase on it.
+struct FullBar {
+  int index;
+  uint32_t parity;
+};
+__device__ __forceinline__ FullBar full_bar(int n, int nslot) {
+  const int s = n % nslot, use = n / nslot;
+  if (nslot % NSTAGE == 0) return {2 * s, uint32_t(use & 1)};
+  return {2 * s + (use & 1), uint32_t((use >> 1) & 1)};
+}
 
 __device__ __forceinline__ float2 unpack2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
 __device__ __forceinline__ float lane4(const float4 &v, int j) {
@@ -454,11 +467,12 @@ __global__ void __launch_bounds__(NT, 1)
     const int h0 = (u / n_tiles) * UK, t0 = (u % n_tiles) * UT + q * QT, s = n % nslot;
     unsigned char *st = ring + s * sbytes;
     if (tc::elect_one()) {
-      tc::mbar_arrive_expect_tx(&full[s], uint32_t(sbytes));
-      tc::tma_load_3d(st, &tm_part, h0, t0, 0, &full[s]);
-      tc::tma_load_3d(st + slot_res(p.tp), &tm_res, h0, 0, t0, &full[s]);
-      tc::tma_load_2d(st + slot_post(p.tp), &tm_post, 0, t0, &full[s]);
-      tc::tma_load_2d(st + slot_comb(p.tp), &tm_comb, 0, t0, &full[s]);
+      uint64_t *bar = &full[full_bar(n, nslot).index];
+      tc::mbar_arrive_expect_tx(bar, uint32_t(sbytes));
+      tc::tma_load_3d(st, &tm_part, h0, t0, 0, bar);
+      tc::tma_load_3d(st + slot_res(p.tp), &tm_res, h0, 0, t0, bar);
+      tc::tma_load_2d(st + slot_post(p.tp), &tm_post, 0, t0, bar);
+      tc::tma_load_2d(st + slot_comb(p.tp), &tm_comb, 0, t0, bar);
     }
     __syncwarp();
   };
@@ -466,7 +480,8 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp == PROD_WARP) {
     if (tc::elect_one()) {
       for (int s = 0; s < nslot; ++s) {
-        tc::mbar_init(&full[s], 1);
+        tc::mbar_init(&full[2 * s], 1);
+        tc::mbar_init(&full[2 * s + 1], 1);
         tc::mbar_init(&empty[s], STAGE_WARPS);
       }
       tc::mbar_init(afull, MIX_WARPS);
@@ -525,7 +540,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     // copies still in flight land before exit
     for (int n = nf - nslot < 0 ? 0 : nf - nslot; n < nf; ++n)
-      tc::mbar_wait_bounded(&full[n % nslot], uint32_t((n / nslot) & 1), WAIT_LIMIT);
+      tc::mbar_wait_bounded(&full[full_bar(n, nslot).index], full_bar(n, nslot).parity, WAIT_LIMIT);
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // a unit's 3 x 8 MMAs once its A operand is complete
@@ -589,7 +604,8 @@ __global__ void __launch_bounds__(NT, 1)
       if (*abort_s) break;
       const int u = u_begin + i, g = u / n_tiles, tile = u % n_tiles;
       const int n = i * NSTAGE + q, s = n % nslot;
-      if (!tc::mbar_wait_bounded(&full[s], uint32_t((n / nslot) & 1), WAIT_LIMIT)) {
+      const FullBar fb = full_bar(n, nslot);
+      if (!tc::mbar_wait_bounded(&full[fb.index], fb.parity, WAIT_LIMIT)) {
         *abort_s = 1;
         break;
       }
