@@ -30,7 +30,7 @@ constexpr int NT = WARPS * 32;
 constexpr int KB = 8;                        // routes loaded per batch
 constexpr int TP_MAX = 32;
 
-__global__ void __launch_bounds__(NT) k_moe_fold(const FoldParams p) {
+__global__ void __launch_bounds__(NT, 4) k_moe_fold(const FoldParams p) {
   extern __shared__ float4 xs[];             // [tp][32][2]: x_r of the chunk's 32 fragments
   const int H = p.hidden, K = p.top_k, nfrag = H / VEC;
   const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(NT) k_moe_fold(const FoldParams p) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] = 0.f;
       if (live) {
+        // the shared expert's row does not depend on the route indices: its
+        // load is in flight with theirs and the routes'
+        const uint4 sv = ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)fr * VEC);
         const int32_t *ix = p.idx + ((size_t)r * p.m + t) * K;
         const float *wt = p.weights + (size_t)t * K;
         const uint16_t *rows = p.routed + (size_t)r * p.rows_per_rank * H + (size_t)fr * VEC;
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(NT) k_moe_fold(const FoldParams p) {
           }
         }
         float s[8];
-        unpack8(ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)fr * VEC), s);
+        unpack8(sv, s);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(x[e], s[e]);
         round8(x);
