@@ -243,6 +243,10 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
   // partial-sum rows (mixes warp): copies issued for tokens < pissued, rows
   // reduced for tokens < preduced
   int pissued = part_bytes ? (slots < n_tok ? slots : n_tok) : 0, preduced = 0;
+  // the pre-mix's scale and base, read once (not after every token's
+  // reduction, where the load would add a round trip to the chain)
+  const float pre_scale = warp == MIX_WARP && !p.pre_in ? p.scale[0] : 0.f;
+  const float pre_base = warp == MIX_WARP && !p.pre_in && lane < HC ? p.base[lane] : 0.f;
   // mixes warp: steps 1-2 for token k of this CTA (its pre into pre_s[k & 1])
   auto token_pre = [&](int k) {
     const int t = int(blockIdx.x) + k * int(gridDim.x);
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
       if (p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
       if (p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
       if (lane < HC) {
-        const float pre = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+        const float pre = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, pre_scale), pre_base)), p.hc_eps);
         pre_s[k & 1][lane] = pre;
         if (p.pre_out) p.pre_out[(size_t)t * HC + lane] = pre;
       }
