@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
                                                ctypes.c_size_t]
         h.mhc_boundary_run_static.restype = st
         h.mhc_mxfp8_scale_bytes.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        h.mhc_test_stall_stage_copies.argtypes = [ctypes.c_int32]
+        h.mhc_test_stall_stage_copies.restype = st
         h.mhc_mxfp8_scale_bytes.restype = ctypes.c_size_t
         h.mhc_boundary_launches_per_call.argtypes = [vp]
         h.mhc_boundary_launches_per_call.restype = ctypes.c_int32
@@ -165,6 +167,14 @@ def mhc_boundary_run_static(config: mhc_boundary_config_t, args: mhc_run_args_t,
                                            err, len(err))
     if status != MHC_OK:
         raise MhcError(status, err.value.decode())
+
+
+def mhc_test_stall_stage_copies(on: bool) -> None:
+    """Test hook (include/mhc_boundary_test.h): the stage kernels launched
+    from now on issue no input copies, so their bounded waits run out."""
+    status = lib().mhc_test_stall_stage_copies(1 if on else 0)
+    if status != MHC_OK:
+        raise MhcError(status, "could not set the stall flag")
 
 
 def mhc_boundary_profile_begin(handle, max_calls: int) -> None:

@@ -25,6 +25,7 @@
 
 #include "launch.cuh"
 #include "mhc_boundary.h"
+#include "mhc_boundary_test.h"
 
 using namespace mhc;
 
@@ -760,3 +761,8 @@ const char *mhc_last_error(const mhc_boundary_t *b) {
 }
 
 }  // extern "C"
+
+mhc_status_t mhc_test_stall_stage_copies(int32_t on) {
+  const cudaError_t e = stage_tc_stall_copies(on ? 1 : 0);
+  return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
+}

@@ -72,6 +72,11 @@
 namespace mhc {
 namespace {
 
+// Test hook (mhc_test_stall_stage_copies): when set, the producer issues no
+// input copies, so the kernel's bounded waits run out and it reports the
+// timeout through the error word instead of hanging.
+__device__ int g_stall_copies = 0;
+
 constexpr int MIX_WARPS = 16;                 // mixer warps
 constexpr int PROD_WARP = MIX_WARPS;          // the TMA producer warp
 constexpr int MMA_WARP = MIX_WARPS + 1;       // the MMA warp
@@ -514,8 +519,9 @@ __global__ void __launch_bounds__(NT, 1)
     // The inputs, and the outputs that the preceding kernel may still read,
     // are touched only after it has completed.
     pdl_wait();
+    const bool stall = *static_cast<volatile int *>(&g_stall_copies) != 0;
     if (gemv && !p.early_weight) stage_hc_fn(p, &tm_fn, first_group, a_s, bfull);
-    for (int n = 0; n < nslot && n < total_fills; ++n) fill(n);
+    for (int n = 0; !stall && n < nslot && n < total_fills; ++n) fill(n);
     // the later groups' weight rows, so that their staging copies read L2
     const int last_group = gemv ? (u_end - 1) / n_tiles : first_group;
     for (int g = first_group + 1; g <= last_group && g <= first_group + 16; ++g) {
@@ -529,8 +535,8 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
     }
     // refill each slot as soon as its previous stage has been read
-    int nf = nslot < total_fills ? nslot : total_fills;
-    for (; nf < total_fills; ++nf) {
+    int nf = stall ? 0 : nslot < total_fills ? nslot : total_fills;
+    for (; !stall && nf < total_fills; ++nf) {
       const int s = nf % nslot;
       if (!tc::mbar_wait_bounded(&empty[s], uint32_t((nf / nslot - 1) & 1), WAIT_LIMIT) || *abort_s) {
         if (lane == 0) *abort_s = 1;
@@ -713,6 +719,10 @@ bool encode(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *ba
 }  // namespace
 
 size_t stage_tc_smem_bytes() { return size_t(SMEM_MAX); }
+
+cudaError_t stage_tc_stall_copies(int on) {
+  return cudaMemcpyToSymbol(g_stall_copies, &on, sizeof on);
+}
 
 cudaError_t stage_tc_set_attributes() {
   if (!encode_fn()) return cudaErrorNotSupported;

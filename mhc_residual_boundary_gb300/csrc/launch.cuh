@@ -119,6 +119,7 @@ cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream);
 // persistent, at most `ctas` CTAs of one per SM.
 size_t stage_tc_smem_bytes();
 cudaError_t stage_tc_set_attributes();
+cudaError_t stage_tc_stall_copies(int on);   // test hook, see include/mhc_boundary_test.h
 cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream);
 // Finish kernel: persistent CTAs (at most `ctas`), programmatic dependent
 // launch after the stage kernel when `pdl`.

@@ -23,7 +23,8 @@ def capi():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    import glob
+    text = "\n".join(open(h).read() for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(mhc_[a-z0-9_]+)\s*\(", text)))
 
