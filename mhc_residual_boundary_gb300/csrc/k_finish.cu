@@ -23,15 +23,21 @@
 //     warps collapse the batch's last token; otherwise the raw mixes go to
 //     `mixes` for the side kernel.
 //
-// Layout on the GPU: persistent CTAs of 256 threads, two per SM where the
-// shared memory allows, each taking tokens blockIdx.x, blockIdx.x + gridDim.x,
-// ...  A token's four new streams are one contiguous 8H-byte run of
-// residual_out and its partial sums one 16-byte-padded row, so each token
-// arrives in shared memory by two bulk copies into a ring of one or two
-// slots; the collapse keeps c in registers (BF16), so thread 0 refills the
-// slot as soon as the collapse has read it and the next token's copies are in
-// flight while this one is normalised and stored.  Every wait is bounded; a wait
-// that gives up sets bit 1 of the error word.
+// Layout on the GPU: persistent CTAs of 256 threads (7 collapse warps and
+// the mixes warp), up to four per SM as the shared memory allows, each
+// taking tokens blockIdx.x, blockIdx.x + gridDim.x, ...  A token's four new
+// streams are one contiguous 8H-byte run of residual_out and its partial
+// sums one 16-byte-padded row, so each token arrives in shared memory by two
+// bulk copies into a ring of one or two slots, each on its own barrier: the
+// mixes warp reduces token k + 1's partial-sum row (and issues the copy of
+// the row that takes its place) while the collapse warps work on token k.
+// The collapse keeps c in registers (BF16 pairs), so thread 0 refills the
+// slot's stream rows as soon as the collapse has read them, and the next
+// token's copy is in flight while this one is normalised and stored; the
+// collapse and normalisation run on FP32 pairs with each operation rounded
+// as written above.  Every wait is bounded; a wait that gives up sets bit 1
+// of the error word, and the CTA's stop decision is the barrier's OR of its
+// threads' failed waits.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
