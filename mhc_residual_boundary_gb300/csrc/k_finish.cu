@@ -65,14 +65,20 @@ static_assert(CT % 4 == 0, "a 32-element MXFP8 block is four consecutive collaps
 __host__ __device__ inline size_t slot_bytes(int hidden, int part_stride) {
   return size_t(HC) * hidden * 2 + size_t(part_stride) * 4;
 }
-// CTAs per SM (up to 4) and ring slots per CTA: as many CTAs as fit with one
-// slot each (more warps and more tokens in flight), then a second slot.
+// CTAs per SM (up to 4) and ring slots per CTA.  Up to DEEP_TOKENS tokens an
+// SM: as many CTAs as fit with one slot each (more warps, and a CTA's first
+// token arrives sooner), then a second slot.  Above it, where each CTA runs a
+// long chain of tokens, two slots a CTA first (each CTA has its next token's
+// copies in flight during the current one's normalisation): at H = 6144 this
+// trades 4 CTAs x 1 slot for 2 x 2, which measured 2 % faster a call at 4096
+// tokens on 152 SMs and 1-2 % slower at 512-1024.
+constexpr int DEEP_TOKENS = 12;
 struct Occupancy {
   int ctas, slots;
 };
-inline Occupancy occupancy(int hidden, int part_stride) {
+inline Occupancy occupancy(int hidden, int part_stride, bool deep) {
   const size_t slot = slot_bytes(hidden, part_stride);
-  int ctas = int(SMEM_SM / slot);
+  int ctas = int(SMEM_SM / (deep ? 2 * slot : slot));
   ctas = ctas < 1 ? 1 : ctas > 4 ? 4 : ctas;
   const int slots = ctas * 2 * slot <= SMEM_SM ? 2 : 1;
   return {ctas, slots};
@@ -459,7 +465,7 @@ cudaError_t finish_set_attributes() {
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl) {
   if (p.hidden % VEC || p.hidden > MAX_HIDDEN || p.part_stride % 4 || p.part_stride < p.slices * VALUES)
     return cudaErrorInvalidValue;
-  const Occupancy occ = occupancy(p.hidden, p.part_stride);
+  const Occupancy occ = occupancy(p.hidden, p.part_stride, p.m >= DEEP_TOKENS * ctas);
   const int slots = occ.slots;
   const size_t smem = size_t(slots) * slot_bytes(p.hidden, p.part_stride);
   if (smem > SMEM_LIMIT) return cudaErrorInvalidValue;
@@ -467,15 +473,16 @@ cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, 
   // persistent: as many CTAs as are resident at once (the runtime's count, so
   // that the static shared memory and the per-CTA reservation are included)
   // (cached per kernel and ring size: the query costs host time on every call)
-  static std::atomic<uint64_t> cache[NFMAX];
-  const uint64_t cached = cache[nf - 1].load(std::memory_order_relaxed);
+  static std::atomic<uint64_t> cache[NFMAX][MAX_SLOTS];
+  std::atomic<uint64_t> &entry = cache[nf - 1][slots - 1];
+  const uint64_t cached = entry.load(std::memory_order_relaxed);
   int resident = 0;
   if (cached && (cached >> 8) == smem) {
     resident = int(cached & 0xff);
   } else {
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kFinish[nf - 1], NT, smem);
     if (e != cudaSuccess) return e;
-    cache[nf - 1].store((uint64_t(smem) << 8) | uint64_t(resident & 0xff), std::memory_order_relaxed);
+    entry.store((uint64_t(smem) << 8) | uint64_t(resident & 0xff), std::memory_order_relaxed);
   }
   resident = resident < 1 ? 1 : resident > occ.ctas ? occ.ctas : resident;
   const int grid = ctas * resident;
