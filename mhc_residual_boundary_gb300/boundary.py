@@ -135,8 +135,7 @@ class Boundary:
             want = shape(self.tp, m, self.hidden, K, rows)
             if t.dtype != dtype or tuple(t.shape) != want or not t.is_contiguous():
                 raise ValueError(f"{n}: expected contiguous {dtype} {want}, got {t.dtype} {tuple(t.shape)}")
-            if (t.device.type == "cuda") != (where == "device"):
-                raise ValueError(f"{n} must be a {where} tensor")
+            self._check_place(n, t, where)
         for n in names:
             if n in capi.RUN_FIELDS:
                 setattr(args, n, inputs[n].data_ptr())
@@ -144,10 +143,18 @@ class Boundary:
             dtype, shape = OUTPUT_SPECS[n]
             if t.dtype != dtype or tuple(t.shape) != shape(m, self.hidden) or not t.is_contiguous():
                 raise ValueError(f"{n}: expected contiguous {dtype} {shape(m, self.hidden)}")
-            if (t.device.type == "cuda") != (where == "device"):
-                raise ValueError(f"{n} must be a {where} tensor")
+            self._check_place(n, t, where)
             setattr(args, n, t.data_ptr())
         return args, rows
+
+    def _check_place(self, n: str, t: torch.Tensor, where: str) -> None:
+        # the kernels dereference every pointer on this boundary's GPU: a
+        # device call takes tensors on that GPU, a host call host tensors
+        if where == "device":
+            if t.device != self.device:
+                raise ValueError(f"{n} must be a tensor on {self.device}, got {t.device}")
+        elif t.device.type != "cpu":
+            raise ValueError(f"{n} must be a host tensor, got {t.device}")
 
     # ---------------------------------------------------------------- calls
     def run(self, inputs: dict, outputs: dict, stream=None) -> dict:
@@ -188,14 +195,16 @@ class Boundary:
             t = inputs[n]
             dtype, shape = INPUT_SPECS[n] if n in INPUT_SPECS else OUTPUT_SPECS[n]
             want = shape(self.tp, m, self.hidden, K, rows) if n in INPUT_SPECS else shape(m, self.hidden)
-            if t.dtype != dtype or tuple(t.shape) != want or not t.is_contiguous() or t.device.type != "cuda":
-                raise ValueError(f"{n}: expected contiguous cuda {dtype} {want}")
+            if t.dtype != dtype or tuple(t.shape) != want or not t.is_contiguous():
+                raise ValueError(f"{n}: expected contiguous {dtype} {want}")
+            self._check_place(n, t, "device")
             setattr(a, n, t.data_ptr())
         a.rows_per_rank = rows
         for n, t in outputs.items():
             dtype, shape = OUTPUT_SPECS[n]
             if t.dtype != dtype or tuple(t.shape) != shape(m, self.hidden) or not t.is_contiguous():
                 raise ValueError(f"{n}: expected contiguous {dtype} {shape(m, self.hidden)}")
+            self._check_place(n, t, "device")
             setattr(a, n, t.data_ptr())
         capi.mhc_boundary_consume(self.handle, a, stream)
         return outputs
