@@ -71,3 +71,21 @@ def test_consumer_and_owner_reduce_bytes():
     owner = bench.call_bytes(bench.workload("owner_reduce", m))
     # the owners' sums: written once, read back once
     assert owner["total"] - direct["total"] == m * 4 * H
+
+
+def test_traffic_is_read_only_for_the_same_workload_and_source(tmp_path, monkeypatch):
+    import hashlib
+    csrc = tmp_path / "mhc_residual_boundary_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k_stage_tc.cu").write_bytes(b"// kernel source\n")
+    sha = hashlib.sha256(b"// kernel source\n").hexdigest()[:12]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k_stage_tc_large.md").write_text(
+        f"traffic: workload=large_mxfp8 tokens=4096 kernel=k_stage_tc source_sha={sha} bytes_per_launch=123\n"
+        f"traffic: workload=glm tokens=256 kernel=k_stage_tc source_sha=000000000000 bytes_per_launch=456\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_traffic(bench.workload("large_mxfp8", 4096)) == 123
+    assert bench.kernel_traffic(bench.workload("large_mxfp8", 2048)) is None     # other size
+    assert bench.kernel_traffic(bench.workload("glm", 256)) is None              # other source
+    (csrc / "k_stage_tc.cu").write_bytes(b"// kernel source, edited\n")
+    assert bench.kernel_traffic(bench.workload("large_mxfp8", 4096)) is None     # stale capture
