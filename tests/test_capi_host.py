@@ -112,3 +112,57 @@ def test_flag_values_match_the_header(capi):
     assert declared, "no flags found in the header"
     bound = {name: getattr(capi, name) for name in dir(capi) if name.startswith("MHC_FLAG_")}
     assert declared == bound
+
+
+def _static_args(capi, m=4):
+    # fake, 16-byte aligned device addresses: every case below is refused by
+    # the host-side checks, before the first CUDA call, so none is dereferenced
+    a = capi.mhc_run_args_t()
+    a.m = m
+    for i, f in enumerate(("partials", "residual", "post", "comb", "hc_fn", "scale", "base", "norm_weight",
+                           "residual_out", "layer_input", "post_out", "comb_out")):
+        setattr(a, f, 0x10000 * (i + 1))
+    return a
+
+
+def _static(capi, cfg, a):
+    import ctypes
+    err = ctypes.create_string_buffer(512)
+    status = capi.lib().mhc_boundary_run_static(ctypes.byref(cfg), ctypes.byref(a), None, err, len(err))
+    return capi.STATUS[status], err.value.decode()
+
+
+@pytest.mark.parametrize("case,status,text", [
+    ("hidden", "MHC_ERR_INVALID_ARG", "hidden must be a positive multiple of 8"),
+    ("owner_flag", "MHC_ERR_UNSUPPORTED", "only MHC_FLAG_MXFP8"),
+    ("m0", "MHC_ERR_CAPACITY", "outside [1, 865]"),
+    ("m_big", "MHC_ERR_CAPACITY", "outside [1, 865]"),
+    ("null", "MHC_ERR_INVALID_ARG", "partials is NULL"),
+    ("misaligned", "MHC_ERR_INVALID_ARG", "residual is not 16-byte aligned"),
+    ("two_weights", "MHC_ERR_INVALID_ARG", "exactly one of hc_fn and hc_fn_bf16"),
+    ("mx_half", "MHC_ERR_INVALID_ARG", "mxfp8_values and mxfp8_scales go together"),
+    ("mx_no_flag", "MHC_ERR_UNSUPPORTED", "MXFP8 outputs need MHC_FLAG_MXFP8"),
+])
+def test_static_entry_refuses_before_any_launch(capi, case, status, text):
+    cfg = capi.mhc_boundary_config_t(6144, 4, 4, 0, 20, 0, 1e-6, 1e-6, 2.0, 1e-6, 0)
+    a = _static_args(capi)
+    if case == "hidden":
+        cfg.hidden = 6140
+    elif case == "owner_flag":
+        cfg.flags = capi.MHC_FLAG_OWNER_REDUCE
+    elif case == "m0":
+        a.m = 0
+    elif case == "m_big":
+        a.m = 866      # the 8 MiB scratch holds 865 tokens at H = 6144
+    elif case == "null":
+        a.partials = None
+    elif case == "misaligned":
+        a.residual += 8
+    elif case == "two_weights":
+        a.hc_fn_bf16 = 0x900000
+    elif case == "mx_half":
+        a.mxfp8_values = 0x900000
+    elif case == "mx_no_flag":
+        a.mxfp8_values, a.mxfp8_scales = 0x900000, 0xA00000
+    got_status, got_text = _static(capi, cfg, a)
+    assert got_status == status and text in got_text, (got_status, got_text)
