@@ -58,7 +58,7 @@ typedef struct CUstream_st *mhc_stream_t;
 typedef enum {
   MHC_OK = 0,
   MHC_ERR_INVALID_ARG = 1, /* a pointer, size, alignment or shape is wrong */
-  MHC_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  MHC_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   MHC_ERR_CAPACITY = 3,    /* m outside [1, max_num_tokens] */
   MHC_ERR_CUDA = 4,        /* a CUDA call failed */
   MHC_ERR_OOM = 5,         /* device allocation failed in create */
