@@ -105,10 +105,13 @@ def test_few_tokens(Boundary, hidden, tp, m, bf16):
 
 
 @pytest.mark.parametrize("hidden,tp,m,bf16", [(2048, 6, 1024, False), (2048, 3, 1024, False),
-                                              (6144, 8, 512, True), (2048, 8, 1024, True)])
+                                              (6144, 8, 512, True), (2048, 8, 1024, True),
+                                              (5120, 8, 2000, False)])
 def test_ring_wraps_many_times(Boundary, hidden, tp, m, bf16):
     # several units per CTA, so every ring slot is reused many times, at tp
-    # values whose slot count is not a multiple of a unit's four stages
+    # values whose slot count is not a multiple of a unit's four stages; the
+    # 2000-token case has more than 12 tokens an SM, where the finish kernel
+    # runs two-slot CTAs, with a ragged share of tokens per CTA
     check(Boundary, hidden, tp, m, bf16_weight=bf16, seed=hidden + tp + m)
 
 
