@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -166,3 +167,21 @@ def test_static_entry_refuses_before_any_launch(capi, case, status, text):
         a.mxfp8_values, a.mxfp8_scales = 0x900000, 0xA00000
     got_status, got_text = _static(capi, cfg, a)
     assert got_status == status and text in got_text, (got_status, got_text)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # a fresh interpreter whose binding points at a library that was never
+    # built: the first use raises, and nothing falls back to a CPU path
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from mhc_residual_boundary_gb300 import capi\n"
+        "capi.LIB_PATH = %r\n"
+        "try:\n"
+        "    capi.mhc_mxfp8_scale_bytes(128, 256)\n"
+        "except ImportError as e:\n"
+        "    print('raised:', e)\n"
+        "else:\n"
+        "    print('no error')\n" % (ROOT, str(tmp_path / "libmhc_boundary.so")))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.startswith("raised:") and "no fallback" in out.stdout
