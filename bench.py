@@ -259,6 +259,21 @@ def oracle_tokens_per_s(w, inputs, tokens, threads):
     return tokens / (time.perf_counter() - t0)
 
 
+def cpu_baseline(w, inputs):
+    """The oracle as it stands, timed on the host cores: every token of the
+    workload once over all cores, and up to 512 tokens on one thread."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    sample = w.m
+    one = min(sample, 512)
+    return {"value": oracle_tokens_per_s(w, inputs, sample, threads), "unit": "tokens/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"all {sample} tokens of the workload once, token ranges over {threads} threads",
+            "single_thread_value": oracle_tokens_per_s(w, inputs, one, 1),
+            "single_thread_sample": f"the first {one} tokens on one thread"}
+
+
 def run_reference(args, w):
     world, rank, _ = dist_info()
     if rank != 0:
@@ -394,18 +409,7 @@ def run_ours(args, w):
         e2e = {"value": job_value(world, w.m, args.e2e_steps, e2e_s), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        import oracle
-        oracle.build()
-        threads = os.cpu_count() or 1
-        sample = w.m
-        one = min(sample, 512)
-        cpu = {"value": oracle_tokens_per_s(w, inputs, sample, threads), "unit": "tokens/s",
-               "cores": threads, "kind": "oracle",
-               "sample": f"all {sample} tokens of the workload once, token ranges over {threads} threads",
-               "single_thread_value": oracle_tokens_per_s(w, inputs, one, 1),
-               "single_thread_sample": f"the first {one} tokens on one thread"}
+    cpu = cpu_baseline(w, inputs) if rank == 0 and world == 1 and not args.no_cpu else None
 
     launches = b.launches_per_call() + (1 if w.moe else 0)
     b.close()

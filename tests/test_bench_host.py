@@ -89,3 +89,12 @@ def test_traffic_is_read_only_for_the_same_workload_and_source(tmp_path, monkeyp
     assert bench.kernel_traffic(bench.workload("glm", 256)) is None              # other source
     (csrc / "k_stage_tc.cu").write_bytes(b"// kernel source, edited\n")
     assert bench.kernel_traffic(bench.workload("large_mxfp8", 4096)) is None     # stale capture
+
+
+def test_cpu_baseline_leg_times_the_oracle():
+    from mhc_residual_boundary_gb300 import synth
+    w = bench.workload("tiny", None)
+    cpu = bench.cpu_baseline(w, synth.inputs_for(w))
+    assert cpu["kind"] == "oracle" and cpu["unit"] == "tokens/s" and cpu["cores"] >= 1
+    assert cpu["value"] > 0 and cpu["single_thread_value"] > 0
+    assert f"all {w.m} tokens" in cpu["sample"]
