@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--m", type=int, default=None, help="token count (default: the workload's largest)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' rows")
     ap.add_argument("--no-static-weight", action="store_true",
                     help="read the prenorm weight only after the preceding kernel (not as a layer weight)")
     ap.add_argument("--sweep", action="store_true",
@@ -388,7 +389,7 @@ def run_ours(args, w):
                 "peak_source": peak_src,
                 "kernel_ms_per_call": {"stage": stage_ms, "finish": prof["finish_ms"] / max(prof["calls"], 1),
                                        "mixes": prof["mixes_ms"] / max(prof["calls"], 1)},
-                "call_gbs": call_gbs, "call_frac": call_gbs / peak,
+                "call_gbs": call_gbs, "call_frac": call_gbs / peak, "call_frac_8tbs": call_gbs / 8000.0,
                 "call_algorithmic_bytes": nbytes["total"]}
 
     # end to end through the host-buffer entry point
@@ -410,6 +411,7 @@ def run_ours(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
 
     cpu = cpu_baseline(w, inputs) if rank == 0 and world == 1 and not args.no_cpu else None
+    pc = per_config(device, peak, l2) if rank == 0 and not args.no_per_config else None
 
     launches = b.launches_per_call() + (1 if w.moe else 0)
     b.close()
@@ -422,127 +424,170 @@ def run_ours(args, w):
             "config": dict(describe(w), l2=(f"inputs larger than L2: {nbytes['total'] / 1e6:.1f} MB per call, "
                                             f"{nsets} buffer set(s) rotated, L2 {l2 / 1e6:.0f} MB"),
                            parallelism=f"replicas x{world}"),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "per_config": pc,
             "gpu_launches": args.steps * launches, "clocks": clock,
         }), flush=True)
     if dist is not None:
         dist.destroy_process_group()
 
 
-def run_sweep(args):
-    """Every workload at every token count: per-call device time over
-    back-to-back calls (buffer sets rotated so that each call reads HBM),
-    achieved algorithmic GB/s against the measured and the nominal 8 TB/s
-    peak, and the per-kernel times of a second, profiled pass."""
+def measure_workload(w, steps, warmup, device, peak, l2, profile=True, latency=False):
+    """One workload: per-call device time over back-to-back calls (buffer sets
+    rotated so that each call reads HBM), from Python stream launches and from
+    a CUDA graph replaying the calls; achieved algorithmic GB/s against the
+    measured and the nominal 8 TB/s peak; per-kernel times of a profiled pass;
+    a hot-L2 replay (labelled as such); with `latency`, the device time of one
+    call on its own (events around a single call after the stream drained)."""
     import numpy as np
+    import torch
+    from mhc_residual_boundary_gb300 import Boundary, synth
+    stream = torch.cuda.current_stream()
+    inputs = synth.inputs_for(w, seed=0)
+    dev_in = {("norm_weight" if k == "gamma" else k):
+              (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
+               else torch.from_numpy(v)).to(device) for k, v in inputs.items()}
+    b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
+                 static_weight=STATIC_WEIGHT, owner_reduce=w.owner, device=device.index)
+    nbytes = call_bytes(w)
+    nsets = 1 if nbytes["total"] >= 3 * l2 else math.ceil(3 * l2 / nbytes["total"]) + 1
+
+    def outputs():
+        o = b.empty_outputs(w.m, mxfp8=w.mxfp8)
+        if w.consume:
+            o = {k: v for k, v in o.items()
+                 if k == "residual_out" or (k == "layer_input" and not w.residual_only)}
+        return o
+    if w.residual_only:
+        dev_in.pop("norm_weight", None)
+    sets = [(dev_in if s == 0 else {k: v.clone() for k, v in dev_in.items()}, outputs())
+            for s in range(nsets)]
+    call = b.consume if w.consume else b.finalize_moe if w.moe else b.run
+    steps = max(steps, nsets)
+    for i in range(max(warmup, 3)):
+        call(*sets[i % nsets], stream=stream)
+    b.join(stream)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        call(*sets[i % nsets], stream=stream)
+    b.join(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(stop) * 1e3 / steps
+    prof = None
+    if profile:
+        b.profile_begin(steps)
+        for i in range(steps):
+            call(*sets[i % nsets], stream=stream)
+        b.join(stream)
+        torch.cuda.synchronize()
+        prof = b.profile_end()
+    # the same calls replayed from a CUDA graph: device time without the
+    # Python binding's per-call host cost
+    graph_us = None
+    if nsets <= 512:
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(nsets):
+                call(*sets[i], stream=cap)
+            b.join(cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // nsets)
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        graph_us = start.elapsed_time(stop) * 1e3 / (reps * nsets)
+        del g
+    # hot L2 (labelled as such): the same graph replay on one buffer set, so
+    # that a workload smaller than L2 reads it from L2
+    hot_us = None
+    if nsets > 1:
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(16):
+                call(*sets[0], stream=cap)
+            b.join(cap)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(1, steps // 16)
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        hot_us = start.elapsed_time(stop) * 1e3 / (reps * 16)
+        del g
+    # one call on its own: the stream drained before it, events around it
+    isolated_us = None
+    if latency:
+        times = []
+        for i in range(200):
+            torch.cuda.synchronize()
+            start.record(stream)
+            call(*sets[i % nsets], stream=stream)
+            b.join(stream)
+            stop.record(stream)
+            torch.cuda.synchronize()
+            times.append(start.elapsed_time(stop) * 1e3)
+        isolated_us = statistics.median(times)
+    b.check_errors()
+    b.close()
+    best = graph_us if graph_us else us
+    gbs = nbytes["total"] / (best * 1e-6) / 1e9
+    res = {"config": describe(w), "us_per_call": best, "tokens_per_s": w.m / (best * 1e-6),
+           "algorithmic_bytes": nbytes["total"], "gbs": gbs, "frac_measured": gbs / peak,
+           "frac_8tbs": gbs / 8000.0, "buffer_sets": nsets, "steps": steps,
+           "timing": "CUDA graph replay of back-to-back calls" if graph_us else "stream launches",
+           "stream_us_per_call": us, "hot_l2_graph_us_per_call": hot_us}
+    if isolated_us is not None:
+        res["isolated_call_us"] = isolated_us
+    if prof:
+        n = max(prof["calls"], 1)
+        res["kernel_us"] = {"stage": prof["stage_ms"] / n * 1e3, "finish": prof["finish_ms"] / n * 1e3,
+                            "mixes": prof["mixes_ms"] / n * 1e3}
+    return res
+
+
+# Workloads reported beside the headline one in every bench line: (name, M)
+PER_CONFIG = [("tiny", 4), ("decode", 64), ("glm", 1), ("glm", 256), ("glm", 512), ("moe", 256)]
+
+
+def per_config(device, peak, l2, steps=2000):
+    out = {}
+    for name, m in PER_CONFIG:
+        w = workload(name, m)
+        r = measure_workload(w, steps, 20, device, peak, l2, profile=False, latency=(name == "glm" and m == 1))
+        out[f"{name}_m{m}"] = {k: r[k] for k in ("us_per_call", "tokens_per_s", "gbs", "frac_measured", "frac_8tbs",
+                                                 "algorithmic_bytes", "buffer_sets", "timing")
+                               } | ({"isolated_call_us": r["isolated_call_us"]} if "isolated_call_us" in r else {})
+    return out
+
+
+def run_sweep(args):
+    """Every workload at every token count (one JSON line each)."""
     import torch
     from __graft_entry__ import build
     build()
-    from mhc_residual_boundary_gb300 import Boundary, synth
+    from mhc_residual_boundary_gb300 import synth
     device = torch.device("cuda", 0)
     peak, _ = measured_peaks()
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
-    stream = torch.cuda.current_stream()
     for name, cands in synth.WORKLOADS.items():
         for w in cands:
-            inputs = synth.inputs_for(w, seed=0)
-            dev_in = {("norm_weight" if k == "gamma" else k):
-                      (torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16
-                       else torch.from_numpy(v)).to(device) for k, v in inputs.items()}
-            b = Boundary(hidden=w.hidden, tp=w.tp, max_num_tokens=w.m, top_k=w.top_k, mxfp8=w.mxfp8,
-                         static_weight=STATIC_WEIGHT, owner_reduce=w.owner)
-            nbytes = call_bytes(w)
-            nsets = 1 if nbytes["total"] >= 3 * l2 else math.ceil(3 * l2 / nbytes["total"]) + 1
-            def outputs():
-                o = b.empty_outputs(w.m, mxfp8=w.mxfp8)
-                if w.consume:
-                    o = {k: v for k, v in o.items()
-                         if k == "residual_out" or (k == "layer_input" and not w.residual_only)}
-                return o
-            if w.residual_only:
-                dev_in.pop("norm_weight", None)
-            sets = [(dev_in if s == 0 else {k: v.clone() for k, v in dev_in.items()}, outputs())
-                    for s in range(nsets)]
-            call = b.consume if w.consume else b.finalize_moe if w.moe else b.run
-            steps = max(args.steps, nsets)
-            for i in range(max(args.warmup, 3)):
-                call(*sets[i % nsets], stream=stream)
-            b.join(stream)
-            torch.cuda.synchronize()
-            start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            start.record(stream)
-            for i in range(steps):
-                call(*sets[i % nsets], stream=stream)
-            b.join(stream)
-            stop.record(stream)
-            torch.cuda.synchronize()
-            us = start.elapsed_time(stop) * 1e3 / steps
-            b.profile_begin(steps)
-            for i in range(steps):
-                call(*sets[i % nsets], stream=stream)
-            b.join(stream)
-            torch.cuda.synchronize()
-            prof = b.profile_end()
-            # the same calls replayed from a CUDA graph: device time without
-            # the Python binding's per-call host cost
-            graph_us = None
-            if nsets <= 512:
-                cap = torch.cuda.Stream()
-                cap.wait_stream(stream)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    for i in range(nsets):
-                        call(*sets[i], stream=cap)
-                    b.join(cap)
-                for _ in range(3):
-                    g.replay()
-                torch.cuda.synchronize()
-                reps = max(1, steps // nsets)
-                start.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                stop.record(stream)
-                torch.cuda.synchronize()
-                graph_us = start.elapsed_time(stop) * 1e3 / (reps * nsets)
-                del g
-            # hot L2 (labelled as such): the same graph replay on one buffer
-            # set, so that a workload smaller than L2 reads it from L2
-            hot_us = None
-            if nsets > 1:
-                cap = torch.cuda.Stream()
-                cap.wait_stream(stream)
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
-                    for _ in range(16):
-                        call(*sets[0], stream=cap)
-                    b.join(cap)
-                for _ in range(3):
-                    g.replay()
-                torch.cuda.synchronize()
-                reps = max(1, steps // 16)
-                start.record(stream)
-                for _ in range(reps):
-                    g.replay()
-                stop.record(stream)
-                torch.cuda.synchronize()
-                hot_us = start.elapsed_time(stop) * 1e3 / (reps * 16)
-                del g
-            b.check_errors()
-            b.close()
-            n = max(prof["calls"], 1)
-            gbs = nbytes["total"] / (us * 1e-6) / 1e9
-            print(json.dumps({
-                "sweep": True, "config": describe(w), "us_per_call": us, "tokens_per_s": w.m / (us * 1e-6),
-                "algorithmic_bytes": nbytes["total"], "gbs": gbs, "frac_measured": gbs / peak,
-                "frac_8tbs": gbs / 8000.0, "buffer_sets": nsets, "steps": steps,
-                "graph_us_per_call": graph_us,
-                "graph_gbs": nbytes["total"] / (graph_us * 1e-6) / 1e9 if graph_us else None,
-                "hot_l2_graph_us_per_call": hot_us,
-                "kernel_us": {"stage": prof["stage_ms"] / n * 1e3, "finish": prof["finish_ms"] / n * 1e3,
-                              "mixes": prof["mixes_ms"] / n * 1e3},
-            }), flush=True)
-            del sets, dev_in
+            r = measure_workload(w, args.steps, args.warmup, device, peak, l2,
+                                 latency=(w.m == 1))
+            print(json.dumps(dict(r, sweep=True)), flush=True)
 
 
 def main():

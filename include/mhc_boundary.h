@@ -101,7 +101,14 @@ enum {
    * more kernel and 4H more bytes a token.  Applies to mhc_boundary_run and
    * to mhc_boundary_consume with partials; a MoE call folds its routes
    * instead. */
-  MHC_FLAG_OWNER_REDUCE = 1u << 5
+  MHC_FLAG_OWNER_REDUCE = 1u << 5,
+  /* mhc_boundary_run_static only (mhc_boundary_create rejects it): after
+   * launching, the call synchronises its stream and reads the error word of
+   * the allocation-free calls on this device, which a kernel sets when one of
+   * its bounded waits gives up; a set word returns MHC_ERR_TIMEOUT (and is
+   * cleared).  Without the flag the word keeps the report until a call with
+   * the flag reads it. */
+  MHC_FLAG_CHECK_ERRORS = 1u << 6
 };
 
 /* Construction arguments ([GLM] AllReduceMhcBoundary.__init__, [DSV]
@@ -302,22 +309,33 @@ size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden);
  * implicit device synchronisation a cudaMalloc / cudaFree can cause, or a
  * thread that may not create a handle (mhc_boundary_create allocates scratch,
  * a stream and events).  It needs no handle: `config` is read as for
- * mhc_boundary_create (top_k is ignored; flags may hold MHC_FLAG_MXFP8 and
- * MHC_FLAG_SYNC_MIXES) and `args` as for mhc_boundary_run, device pointers
- * the caller allocated and owns.  All three kernels run on `stream` in order,
- * so post_out / comb_out need no join.
+ * mhc_boundary_create (top_k is ignored) and `args` as for mhc_boundary_run,
+ * device pointers the caller allocated and owns.  config->flags may hold:
+ *   MHC_FLAG_MXFP8          accept mxfp8_values / mxfp8_scales;
+ *   MHC_FLAG_STATIC_WEIGHT  the prenorm weight is a layer weight: the stage
+ *                           kernel reads it before it waits for the kernel
+ *                           ahead of it on `stream`, so no kernel enqueued
+ *                           before the call may write hc_fn / hc_fn_bf16;
+ *   MHC_FLAG_SYNC_MIXES     accepted and without effect here: post / Sinkhorn
+ *                           always run in a separate kernel on `stream`;
+ *   MHC_FLAG_CHECK_ERRORS   synchronise and report device-side failures (see
+ *                           the flag).
+ * The stage kernel, the finish kernel and the post / Sinkhorn kernel run on
+ * `stream` in order, so post_out / comb_out need no join.
  * Scratch: an 8 MiB array of this library's device memory, which every GPU
  * that loads the library holds until the process exits; a call needs
  * m * (4 * ceil(25 * ceil(H / 64) / 4) + 24) * 4 + 256 bytes of it (H = 6144: up to 865 tokens),
  * and a larger m returns MHC_ERR_CAPACITY with nothing launched.  Every call
  * on a device shares that array and it keeps the last call's contents
- * (nothing needs clearing: each call writes every word it reads before
- * reading it), so calls whose kernels overlap on the GPU race: order them on
- * one stream or with events.  The first call on a device looks up the
- * array's device address and sets a kernel attribute there; make that first
- * call before any stream capture.  Runs on the current device.  On failure
- * the message is written to error[0 .. error_len-1] (error may be NULL) and
- * nothing is launched. */
+ * (nothing needs clearing: each call writes every scratch word it reads
+ * before reading it, unless one of its kernels gave up a bounded wait, which
+ * the error word records), so calls whose kernels overlap on the GPU race:
+ * order them on one stream or with events.  The first call on a device looks
+ * up the addresses of the array and of the error word and sets kernel
+ * attributes there; make that first call before any stream capture.  Runs on
+ * the current device.  On failure the message is written to
+ * error[0 .. error_len-1] (error may be NULL) and nothing is launched, except
+ * for the report of MHC_FLAG_CHECK_ERRORS, which comes after the launches. */
 mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *config, const mhc_run_args_t *args,
                                      mhc_stream_t stream, char *error, size_t error_len);
 

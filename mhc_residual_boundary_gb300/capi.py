@@ -23,6 +23,7 @@ MHC_FLAG_HOST_STAGING = 1 << 2
 MHC_FLAG_SIDE_MIXES = 1 << 3
 MHC_FLAG_STATIC_WEIGHT = 1 << 4
 MHC_FLAG_OWNER_REDUCE = 1 << 5
+MHC_FLAG_CHECK_ERRORS = 1 << 6
 
 
 class MhcError(RuntimeError):

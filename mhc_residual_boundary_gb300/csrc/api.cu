@@ -274,7 +274,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   sp.part = b->part;
   sp.part_stride = part_row_floats(sp.slices);
   sp.err = b->err;
-  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, false, stream);
+  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
   if (ev) {
     cudaEventRecord(ev[1], stream);

@@ -3,9 +3,7 @@
 // One CTA owns a hidden slice of SLICE = 64 columns for a tile of T tokens:
 //   phase A  (thread = token x 16-byte fragment): stage-1 sum of the tp BF16
 //            partials in FP32 in rank order, rounded to BF16 ([DSV]
-//            _LamportMHCDeviceKernel.kernel, lane_sum), or the MoE fold of
-//            routed rows + shared expert per rank ([DSV]
-//            _QuadFinalizePublishDeviceKernel.kernel); then the post-mix of
+//            _LamportMHCDeviceKernel.kernel, lane_sum); then the post-mix of
 //            the four residual streams ([GLM] _BoundaryDeviceKernel.kernel,
 //            "mixed"), written to residual_out and to shared memory, and the
 //            slice's sum of squares of the new streams;
@@ -38,14 +36,14 @@ struct StageLayout {
   static constexpr size_t mixs = news + news_bytes;
   static constexpr size_t mixs_bytes = size_t(T) * MIX_LD * 4;
   static constexpr size_t ss = mixs + mixs_bytes;
-  static constexpr size_t moe = ss + size_t(T) * 4;   // idx [T][tp][K] then w [T][K]
+  static constexpr size_t end = ss + size_t(T) * 4;
   // the GEMV partials of every warp reuse the fn_s / new_s region
   static constexpr size_t red_bytes = size_t(T / 4) * T * MIX * 4;
   static_assert(red_bytes <= fn_bytes + news_bytes, "reduction scratch must fit");
   static_assert(news % 16 == 0 && mixs % 16 == 0, "alignment");
 };
 
-template <int T, bool MOE>
+template <int T>
 __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
   constexpr int NT = T * 8;         // one thread per (token, fragment)
   constexpr int WARPS = NT / 32;
@@ -57,8 +55,6 @@ __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
   uint16_t *new_s = reinterpret_cast<uint16_t *>(smem + L::news);
   float *mix_s = reinterpret_cast<float *>(smem + L::mixs);
   float *ss_s = reinterpret_cast<float *>(smem + L::ss);
-  int *idx_s = reinterpret_cast<int *>(smem + L::moe);
-  float *w_s = reinterpret_cast<float *>(smem + L::moe) + size_t(T) * p.tp * p.top_k;
 
   const int tid = threadIdx.x;
   const int slice = blockIdx.x;
@@ -85,28 +81,6 @@ __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
     if (t < p.m) v = c < HC ? p.post[(size_t)t * HC + c] : p.comb[(size_t)t * HC * HC + (c - HC)];
     mix_s[e] = v;
   }
-  if constexpr (MOE) {
-    // route rows and weights of the tile; an index outside [-1, rows) is
-    // reported and then treated as a route the rank does not hold
-    const int per_token = p.tp * p.top_k;
-    for (int e = tid; e < T * per_token; e += NT) {
-      const int tl = e / per_token, rem = e % per_token;
-      const int r = rem / p.top_k, k = rem % p.top_k, t = t0 + tl;
-      int row = -1;
-      if (t < p.m) {
-        row = p.idx[((size_t)r * p.m + t) * p.top_k + k];
-        if (row < -1 || row >= p.rows_per_rank) {
-          atomicOr(p.err, 1u);
-          row = -1;
-        }
-      }
-      idx_s[e] = row;
-    }
-    for (int e = tid; e < T * p.top_k; e += NT) {
-      const int tl = e / p.top_k, k = e % p.top_k, t = t0 + tl;
-      w_s[e] = t < p.m ? p.weights[(size_t)t * p.top_k + k] : 0.f;
-    }
-  }
   __syncthreads();
 
   // ---- phase A: one thread per (token, fragment of 8 columns)
@@ -118,44 +92,14 @@ __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
   float ss = 0.f;
   if (act) {
     float y[8];
-    if constexpr (!MOE) {
-      // stage 1: acc = +0, then + rank 0, + rank 1, ... (one FP32 add each)
+    // stage 1: acc = +0, then + rank 0, + rank 1, ... (one FP32 add each)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
-      for (int r = 0; r < p.tp; ++r) {
-        float x[8];
-        unpack8(ld_stream(p.partials + ((size_t)r * p.m + t) * H + h), x);
+    for (int e = 0; e < 8; ++e) y[e] = 0.f;
+    for (int r = 0; r < p.tp; ++r) {
+      float x[8];
+      unpack8(ld_stream(p.partials + ((size_t)r * p.m + t) * H + h), x);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], x[e]);
-      }
-    } else {
-      // per rank: sum_k w_k * row_k as fused multiply-adds in k order, plus
-      // the shared expert, rounded to BF16; then the rank-order sum
-      const int *ix = idx_s + tl * p.tp * p.top_k;
-      const float *ww = w_s + tl * p.top_k;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = 0.f;
-      for (int r = 0; r < p.tp; ++r) {
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int k = 0; k < p.top_k; ++k) {
-          const int row = ix[r * p.top_k + k];
-          if (row == -1) continue;
-          float x[8];
-          unpack8(ld_stream(p.routed + ((size_t)r * p.rows_per_rank + row) * H + h), x);
-          const float w = ww[k];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[e] = __fmaf_rn(x[e], w, acc[e]);
-        }
-        float s[8];
-        unpack8(ld_stream(p.shared + ((size_t)r * p.m + t) * H + h), s);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], s[e]);
-        round8(acc);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], acc[e]);
-      }
+      for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], x[e]);
     }
     const uint4 yb = round8(y);
     if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * H + h, yb);
@@ -250,18 +194,16 @@ __global__ void __launch_bounds__(T * 8) k_stage(const StageParams p) {
   }
 }
 
-template <int T, bool MOE>
+template <int T>
 cudaError_t launch_t(const StageParams &p, cudaStream_t stream) {
   const dim3 grid(p.slices, (p.m + T - 1) / T);
-  const size_t smem = stage_smem_bytes(T, MOE, p.tp, p.top_k);
-  k_stage<T, MOE><<<grid, T * 8, smem, stream>>>(p);
+  k_stage<T><<<grid, T * 8, stage_smem_bytes(T), stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int T, bool MOE>
+template <int T>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(k_stage<T, MOE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(STAGE_SMEM_LIMIT));
+  return cudaFuncSetAttribute(k_stage<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(STAGE_SMEM_LIMIT));
 }
 
 }  // namespace
@@ -274,32 +216,26 @@ int stage_tile_tokens(int m) {
   return 32;
 }
 
-size_t stage_smem_bytes(int tile_tokens, bool moe, int tp, int top_k) {
-  size_t base = 0;
+size_t stage_smem_bytes(int tile_tokens) {
   switch (tile_tokens) {
-    case 8: base = StageLayout<8>::moe; break;
-    case 16: base = StageLayout<16>::moe; break;
-    default: base = StageLayout<32>::moe; break;
+    case 8: return StageLayout<8>::end;
+    case 16: return StageLayout<16>::end;
+    default: return StageLayout<32>::end;
   }
-  if (moe) base += size_t(tile_tokens) * (size_t(tp) * top_k + top_k) * 4;
-  return base;
 }
 
 cudaError_t stage_set_attributes() {
   cudaError_t e;
-  if ((e = set_attr<8, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<16, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<32, false>()) != cudaSuccess) return e;
-  if ((e = set_attr<8, true>()) != cudaSuccess) return e;
-  if ((e = set_attr<16, true>()) != cudaSuccess) return e;
-  return set_attr<32, true>();
+  if ((e = set_attr<8>()) != cudaSuccess) return e;
+  if ((e = set_attr<16>()) != cudaSuccess) return e;
+  return set_attr<32>();
 }
 
-cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream) {
+cudaError_t launch_stage(const StageParams &p, cudaStream_t stream) {
   switch (stage_tile_tokens(p.m)) {
-    case 8: return moe ? launch_t<8, true>(p, stream) : launch_t<8, false>(p, stream);
-    case 16: return moe ? launch_t<16, true>(p, stream) : launch_t<16, false>(p, stream);
-    default: return moe ? launch_t<32, true>(p, stream) : launch_t<32, false>(p, stream);
+    case 8: return launch_t<8>(p, stream);
+    case 16: return launch_t<16>(p, stream);
+    default: return launch_t<32>(p, stream);
   }
 }
 

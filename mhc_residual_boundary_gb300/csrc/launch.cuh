@@ -27,16 +27,12 @@ constexpr size_t STAGE_SMEM_LIMIT = 200 * 1024;
 // Largest hidden size the finish kernel's register tiling covers.
 constexpr int MAX_HIDDEN = 16384;
 
-// Stage kernel: stage-1 sum (or MoE fold), post-mix, partial GEMV + sum of
-// squares for one (token tile, hidden slice).
+// Stage kernel: stage-1 sum, post-mix, partial GEMV + sum of squares for one
+// (token tile, hidden slice).  A MoE call's fold kernel runs first and the
+// stage kernel takes its output as the one partial.
 struct StageParams {
   int m, hidden, tp, slices;
   const uint16_t *partials;   // [tp][m][H]
-  const uint16_t *routed;     // [tp][rows][H]      (MoE)
-  const int32_t *idx;         // [tp][m][K]         (MoE)
-  const float *weights;       // [m][K]             (MoE)
-  const uint16_t *shared;     // [tp][m][H]         (MoE)
-  int top_k, rows_per_rank;   //                    (MoE)
   const uint16_t *residual;   // [m][4][H]
   const float *post;          // [m][4]
   const float *comb;          // [m][4][4]
@@ -51,8 +47,7 @@ struct StageParams {
   uint16_t *reduced_out;      // [m][H] or null
   float *part;                // [m][part_stride]: [slices][25] partial GEMV outputs + sum of squares
   int part_stride;            // floats per token row of part (part_row_floats(slices))
-  unsigned int *err;          // device error word (bit 0: bad route index,
-                              // bit 1: a tensor-core completion wait gave up)
+  unsigned int *err;          // device error word (bit 1: a bounded wait gave up), or null
 };
 
 // Finish kernel: per token, the partial sums, mixes, pre, collapse, RMSNorm,
@@ -112,9 +107,9 @@ struct MixesParams {
 
 // Token tile of the stage kernel for a call of m tokens.
 int stage_tile_tokens(int m);
-size_t stage_smem_bytes(int tile_tokens, bool moe, int tp, int top_k);
+size_t stage_smem_bytes(int tile_tokens);
 cudaError_t stage_set_attributes();
-cudaError_t launch_stage(const StageParams &p, bool moe, cudaStream_t stream);
+cudaError_t launch_stage(const StageParams &p, cudaStream_t stream);
 // Stage kernel with the GEMV on tcgen05 tensor cores (non-MoE calls):
 // persistent, at most `ctas` CTAs of one per SM.
 size_t stage_tc_smem_bytes();

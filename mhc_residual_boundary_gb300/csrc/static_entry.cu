@@ -6,17 +6,18 @@
 // code that must not trigger the implicit device synchronisation a
 // cudaMalloc / cudaFree can cause, or a host thread that may not create a
 // handle (mhc_boundary_create allocates its scratch, a side stream and
-// events).  This entry point runs the same three kernels as
-// mhc_boundary_run, all on the caller's stream, with their scratch (the
-// per-slice GEMV partial sums and the raw mixes) in a fixed-size array of
-// this library's device memory instead of memory the handle allocated.
+// events).  This entry point runs the stage kernel, the finish kernel and the
+// separate post / Sinkhorn kernel, all on the caller's stream, with their
+// scratch (the per-group GEMV partial sums and the raw mixes) in a
+// fixed-size array of this library's device memory instead of memory a
+// handle allocated.
 //
-// The array is a file-scope __device__ variable: every GPU that loads this
-// library holds STATIC_SCRATCH_BYTES of it until the process exits.  In host
-// code its name is only a host-side stand-in, never a device address, so the
-// host asks the runtime for the device address (cudaGetSymbolAddress) once
-// per device, with that device current, and passes that pointer to the
-// kernels.
+// The array and the error word are file-scope __device__ variables: every
+// GPU that loads this library holds STATIC_SCRATCH_BYTES of them until the
+// process exits.  In host code their names are only host-side stand-ins,
+// never device addresses, so the host asks the runtime for the device
+// addresses (cudaGetSymbolAddress) once per device, with that device
+// current, and passes those pointers to the kernels.
 #include <atomic>
 #include <cstdarg>
 #include <cstdint>
@@ -33,11 +34,16 @@ namespace {
 // Scratch of every call: [m] rows of partial sums ([slices][25] padded to a
 // multiple of 4 floats), then [m][24] mixes.
 constexpr size_t STATIC_SCRATCH_BYTES = size_t(8) << 20;   // 8 MiB per device
-__device__ __align__(256) float g_scratch[STATIC_SCRATCH_BYTES / sizeof(float)];
+static __device__ __align__(256) float g_scratch[STATIC_SCRATCH_BYTES / sizeof(float)];
+// Error word of the allocation-free calls: bit 1 is set by a stage or finish
+// kernel whose bounded wait gave up (its outputs are then invalid).  It stays
+// set until a call with MHC_FLAG_CHECK_ERRORS reads and clears it.
+static __device__ unsigned int g_static_err;
 
 constexpr int MAX_DEVICES = 64;
 std::mutex g_setup_mutex;
 std::atomic<float *> g_scratch_ptr[MAX_DEVICES];
+unsigned int *g_err_ptr[MAX_DEVICES];
 int g_sm_count[MAX_DEVICES];
 
 mhc_status_t report(char *error, size_t error_len, mhc_status_t status, const char *fmt, ...) {
@@ -52,10 +58,10 @@ mhc_status_t report(char *error, size_t error_len, mhc_status_t status, const ch
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Device address of g_scratch on the current device, looked up once per
-// device; the first call on a device also raises the stage kernels' shared
-// memory limits there and reads its SM count.
-mhc_status_t scratch_on_device(int device, float **out, char *error, size_t error_len) {
+// Device addresses of g_scratch and g_static_err on the current device,
+// looked up once per device; the first call on a device also raises the
+// stage kernels' shared memory limits there and reads its SM count.
+mhc_status_t scratch_on_device(int device, float **out, unsigned int **err, char *error, size_t error_len) {
   if (device < 0 || device >= MAX_DEVICES)
     return report(error, error_len, MHC_ERR_UNSUPPORTED, "device %d is beyond the %d devices supported",
                   device, MAX_DEVICES);
@@ -64,8 +70,9 @@ mhc_status_t scratch_on_device(int device, float **out, char *error, size_t erro
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     ptr = g_scratch_ptr[device].load(std::memory_order_relaxed);
     if (!ptr) {
-      void *addr = nullptr;
+      void *addr = nullptr, *err_addr = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&addr, g_scratch);
+      if (e == cudaSuccess) e = cudaGetSymbolAddress(&err_addr, g_static_err);
       if (e == cudaSuccess) e = stage_set_attributes();
       if (e == cudaSuccess) e = stage_tc_set_attributes();
       if (e == cudaSuccess) e = finish_set_attributes();
@@ -73,10 +80,12 @@ mhc_status_t scratch_on_device(int device, float **out, char *error, size_t erro
       if (e != cudaSuccess)
         return report(error, error_len, MHC_ERR_CUDA, "set-up on device %d: %s", device, cudaGetErrorString(e));
       ptr = static_cast<float *>(addr);
+      g_err_ptr[device] = static_cast<unsigned int *>(err_addr);
       g_scratch_ptr[device].store(ptr, std::memory_order_release);
     }
   }
   *out = ptr;
+  *err = g_err_ptr[device];
   return MHC_OK;
 }
 
@@ -94,9 +103,9 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   if (c.tp < 1 || c.tp > 32) return report(error, error_len, MHC_ERR_INVALID_ARG, "tp must be in [1, 32]");
   if (c.sinkhorn_repeat < 1 || c.sinkhorn_repeat > 10000)
     return report(error, error_len, MHC_ERR_INVALID_ARG, "sinkhorn_repeat must be in [1, 10000]");
-  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_STATIC_WEIGHT))
+  if (c.flags & ~uint32_t(MHC_FLAG_MXFP8 | MHC_FLAG_SYNC_MIXES | MHC_FLAG_STATIC_WEIGHT | MHC_FLAG_CHECK_ERRORS))
     return report(error, error_len, MHC_ERR_UNSUPPORTED,
-                  "only MHC_FLAG_MXFP8, MHC_FLAG_SYNC_MIXES and MHC_FLAG_STATIC_WEIGHT apply");
+                  "only MHC_FLAG_MXFP8, MHC_FLAG_SYNC_MIXES, MHC_FLAG_STATIC_WEIGHT and MHC_FLAG_CHECK_ERRORS apply");
   if ((c.flags & MHC_FLAG_MXFP8) && c.hidden % 128)
     return report(error, error_len, MHC_ERR_INVALID_ARG, "MXFP8 output needs hidden %% 128 == 0");
 
@@ -140,10 +149,12 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   float *scratch = nullptr;
-  const mhc_status_t s = scratch_on_device(device, &scratch, error, error_len);
+  unsigned int *err = nullptr;
+  const mhc_status_t s = scratch_on_device(device, &scratch, &err, error, error_len);
   if (s != MHC_OK) return s;
   // every scratch word a kernel reads was written earlier in the same call,
-  // so nothing needs clearing between calls
+  // so nothing needs clearing between calls (the error word is cleared only
+  // when it is read, below)
   float *part = scratch;
   // the tensor-core stage kernel writes one partial group per 128 columns,
   // the CUDA-core one per 64; the capacity rule above counts the latter
@@ -169,8 +180,8 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
   sp.part = part;
   sp.part_stride = part_row_floats(groups);
-  sp.err = nullptr;   // read only by the MoE variant, which this entry point does not run
-  e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream) : launch_stage(sp, false, stream);
+  sp.err = err;   // a stage-kernel wait that gives up sets bit 1
+  e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream) : launch_stage(sp, stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
 
   FinishParams fp = {};
@@ -186,6 +197,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   fp.rms_eps = c.rms_eps;
   fp.hc_eps = c.hc_eps;
   fp.norm_eps = c.norm_eps;
+  fp.err = err;
   fp.mixes = mixes;
   fp.mixes_out = a->mixes_out;
   fp.pre_out = a->pre_out;
@@ -207,5 +219,18 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   mp.comb_out = a->comb_out;
   e = launch_mixes(mp, stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "mixes kernel: %s", cudaGetErrorString(e));
+  if (!(c.flags & MHC_FLAG_CHECK_ERRORS)) return MHC_OK;
+
+  // the caller asked for the kernels' own failure reports: wait for this call
+  // and read (then clear) the error word of this and earlier calls
+  unsigned int word = 0;
+  e = cudaMemcpyAsync(&word, err, sizeof word, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && word) e = cudaMemsetAsync(err, 0, sizeof word, stream);
+  if (e == cudaSuccess && word) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "error check: %s", cudaGetErrorString(e));
+  if (word & 2u)
+    return report(error, error_len, MHC_ERR_TIMEOUT,
+                  "a kernel gave up one of its bounded waits; the outputs of the call that set it are not valid");
   return MHC_OK;
 }

@@ -1,10 +1,16 @@
 """Shared helpers of the GPU tests: run the CUDA path through the C ABI on
 NumPy inputs and compare every output with the oracle."""
+import os
+
 import numpy as np
 import torch
 
 import oracle
-from tolerances import close_f32, layer_input_ok, ulp_diff
+from tolerances import close_f32, floor_use, floor_use_allowed, layer_input_ok, ulp_diff
+
+# (test id, report) of every comparison in this process; the terminal summary
+# of tests/conftest.py prints how often the layer-input floor was needed
+REPORTS = []
 
 BF16_INPUTS = ("partials", "residual", "norm_weight", "routed", "shared")
 
@@ -66,6 +72,10 @@ def compare(got: dict, ref: dict, inputs: dict, *, mxfp8=False) -> dict:
                         inputs["gamma"])
     report["layer_input_max_ulp"] = int(ulp_diff(got["layer_input"], ref["layer_input"]).max())
     assert ok.all(), f"layer input outside tolerance at {np.argwhere(~ok)[:5].tolist()}"
+    fu = floor_use(got["layer_input"], ref["layer_input"], ref["residual_out"], ref["pre"], inputs["gamma"])
+    report.update({"layer_input_" + k: v for k, v in fu.items()})
+    REPORTS.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], report))
+    assert floor_use_allowed(fu), f"layer input needs the cancellation floor too often: {fu}"
     for name, rname, atol in (("pre_out", "pre", 1e-6), ("post_out", "post_out", 1e-6),
                               ("comb_out", "comb_out", 1e-6), ("mixes_out", "mixes", 1e-5)):
         if name in got:
