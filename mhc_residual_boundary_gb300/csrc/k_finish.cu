@@ -84,118 +84,6 @@ inline Occupancy occupancy(int hidden, int part_stride, bool deep) {
   return {ctas, slots};
 }
 
-__device__ __forceinline__ float sigmoid(float z) {
-  return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-}
-
-// UE8M0 code of the smallest power of two >= s (s >= 0), clamped to [0, 254].
-__device__ __forceinline__ uint32_t ue8m0_ceil(float s) {
-  const uint32_t bits = __float_as_uint(s);
-  const uint32_t ex = bits >> 23, man = bits & 0x7fffffu;
-  uint32_t e;
-  if (bits == 0u) e = 0u;
-  else if (ex == 0u) e = man > (1u << 22) ? 1u : 0u;   // subnormal s
-  else e = ex + (man != 0u ? 1u : 0u);
-  return e > 254u ? 254u : e;
-}
-
-// 2^(127 - e) as an FP32 (normal for e < 254, 2^-127 otherwise).
-__device__ __forceinline__ float inv_scale(uint32_t e) {
-  return e < 254u ? __uint_as_float((254u - e) << 23) : __uint_as_float(0x00400000u);
-}
-
-// A BF16 pair as FP32 (exact).
-__device__ __forceinline__ float2 pair(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
-
-// Lane-wise maximum of two BF16 pairs (finite, non-negative here).
-__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-  unsigned short lo, hi;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return uint32_t(lo) | (uint32_t(hi) << 16);
-}
-
-__device__ __forceinline__ size_t swizzle_128x4(int row, int col, int cols) {
-  const size_t tile = size_t(row / 128) * (cols / 4) + col / 4;
-  const int r = row % 128;
-  return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + (col % 4);
-}
-
-// Next boundary's post-mix and Sinkhorn residual mix of one token, from its
-// normalised mixes, in one thread ([GLM] _MixesDeviceKernel):
-//   post_j = sigmoid(mixes_{4+j} * scale[1] + base[4+j]) * post_mult
-//   logits c[r][k] = mixes_{8+4r+k} * scale[2] + base[8+4r+k]
-//   rows: c = exp(c - max_k c) / sum_k + eps
-//   `repeat` rounds: (from the second round) rows c /= (row sum + eps);
-//                    columns c /= (column sum + eps)
-// with the four-term sums paired ((a + b) + (c + d)) and reciprocals
-// multiplied in.  The reciprocals are CUDA's fast approximate division
-// (within 2 ulp of 1/x for these positive sums), the same operations as the
-// side-stream kernel, so both give the same bits.
-__device__ __forceinline__ float rcp_fast(float x) { return __fdividef(1.0f, x); }
-__device__ __forceinline__ float sum4(float a, float b, float c, float d) {
-  return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
-}
-
-// Its arguments are values, not the kernel's parameter block by reference
-// (an out-of-line function would read that through a generic pointer into
-// parameter space, which is slow).
-struct MixArgs {
-  const float *scale, *base;
-  float *post_out, *comb_out;
-  float post_mult, eps;
-  int repeat;
-};
-
-__device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, const float *mix) {
-#pragma unroll
-  for (int j = 0; j < HC; ++j) {
-    const float z = __fadd_rn(__fmul_rn(mix[HC + j], p.scale[1]), p.base[HC + j]);
-    p.post_out[(size_t)t * HC + j] = __fmul_rn(sigmoid(z), p.post_mult);
-  }
-  const float eps = p.eps, s2 = p.scale[2];
-  float c[HC * HC];
-#pragma unroll
-  for (int i = 0; i < HC * HC; ++i) c[i] = __fadd_rn(__fmul_rn(mix[2 * HC + i], s2), p.base[2 * HC + i]);
-#pragma unroll
-  for (int r = 0; r < HC; ++r) {
-    float *x = c + HC * r;
-    const float peak = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-    for (int k = 0; k < HC; ++k) x[k] = expf(__fsub_rn(x[k], peak));
-    const float inv = rcp_fast(sum4(x[0], x[1], x[2], x[3]));
-#pragma unroll
-    for (int k = 0; k < HC; ++k) x[k] = __fadd_rn(__fmul_rn(x[k], inv), eps);
-  }
-#pragma unroll 1
-  for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) {
-#pragma unroll
-      for (int r = 0; r < HC; ++r) {
-        float *x = c + HC * r;
-        const float inv = rcp_fast(__fadd_rn(sum4(x[0], x[1], x[2], x[3]), eps));
-#pragma unroll
-        for (int k = 0; k < HC; ++k) x[k] = __fmul_rn(x[k], inv);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < HC; ++k) {
-      const float inv = rcp_fast(__fadd_rn(sum4(c[k], c[HC + k], c[2 * HC + k], c[3 * HC + k]), eps));
-#pragma unroll
-      for (int r = 0; r < HC; ++r) c[HC * r + k] = __fmul_rn(c[HC * r + k], inv);
-    }
-  }
-  float *dst = p.comb_out + (size_t)t * HC * HC;
-#pragma unroll
-  for (int i = 0; i < HC * HC; ++i) dst[i] = c[i];
-}
-
 // NF: 16-byte fragments of a row per collapse thread (ceil(H / 8 / 224)).
 // The register bound follows the CTAs per SM that the shared memory allows
 // at that width (a slot is 8H bytes and more): 4 up to NF = 5, then 3, 2, 1.
@@ -351,11 +239,11 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
           uint32_t c[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 a = __fadd2_rn(__fmul2_rn(pair(n0[e]), pre2[0]), __fmul2_rn(pair(n1[e]), pre2[1]));
-            const float2 b = __fadd2_rn(__fmul2_rn(pair(n2[e]), pre2[2]), __fmul2_rn(pair(n3[e]), pre2[3]));
+            const float2 a = __fadd2_rn(__fmul2_rn(bf16_pair(n0[e]), pre2[0]), __fmul2_rn(bf16_pair(n1[e]), pre2[1]));
+            const float2 b = __fadd2_rn(__fmul2_rn(bf16_pair(n2[e]), pre2[2]), __fmul2_rn(bf16_pair(n3[e]), pre2[3]));
             const float2 v = __fadd2_rn(a, b);
             c[e] = pack_bf16x2(v.x, v.y);
-            const float2 r = pair(c[e]);   // the rounded value, as stored
+            const float2 r = bf16_pair(c[e]);   // the rounded value, as stored
             ss2 = __ffma2_rn(r, r, ss2);
           }
           cfr[i] = make_uint4(c[0], c[1], c[2], c[3]);
@@ -394,7 +282,7 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
         if (live) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 o = __fmul2_rn(__fmul2_rn(pair(cw[e]), ir2), pair(gv[e]));
+            const float2 o = __fmul2_rn(__fmul2_rn(bf16_pair(cw[e]), ir2), bf16_pair(gv[e]));
             ow[e] = pack_bf16x2(o.x, o.y);
           }
           st_vec(p.layer_input + (size_t)t * H + (size_t)fr * VEC, make_uint4(ow[0], ow[1], ow[2], ow[3]));
@@ -409,8 +297,8 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
           const uint32_t e8 = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
           const float2 inv2 = make_float2(inv_scale(e8), inv_scale(e8));
           if (live) {
-            const float2 q0 = __fmul2_rn(pair(ow[0]), inv2), q1 = __fmul2_rn(pair(ow[1]), inv2);
-            const float2 q2 = __fmul2_rn(pair(ow[2]), inv2), q3 = __fmul2_rn(pair(ow[3]), inv2);
+            const float2 q0 = __fmul2_rn(bf16_pair(ow[0]), inv2), q1 = __fmul2_rn(bf16_pair(ow[1]), inv2);
+            const float2 q2 = __fmul2_rn(bf16_pair(ow[2]), inv2), q3 = __fmul2_rn(bf16_pair(ow[3]), inv2);
             uint2 q;
             q.x = e4m3x4(q0.x, q0.y, q1.x, q1.y);
             q.y = e4m3x4(q2.x, q2.y, q3.x, q3.y);

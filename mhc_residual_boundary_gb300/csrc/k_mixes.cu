@@ -28,17 +28,6 @@ constexpr int NT = 128;
 constexpr int LANES = HC * HC;             // lanes per token
 constexpr int TOKENS = NT / LANES;         // tokens per CTA
 
-__device__ __forceinline__ float sigmoid(float z) {
-  return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
-}
-
-// The normalisation reciprocals of the Sinkhorn rounds: CUDA's fast
-// approximate division (within 2 ulp of 1/x for the positive sums here).  The
-// rounds form one long dependent chain per token, and the correctly rounded
-// reciprocal made up a fifth of the kernel's time; the result stays within
-// the comb tolerance (rel 1e-4) of the oracle's rounded 1/x.
-__device__ __forceinline__ float recip(float x) { return __fdividef(1.0f, x); }
-
 // Paired four-term sum over the lanes that differ in bits a and 2a.
 __device__ __forceinline__ float sum4(float x, int a) {
   const float s = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, a));
@@ -61,10 +50,10 @@ __global__ void __launch_bounds__(NT) k_mixes(const MixesParams p) {
   float peak = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
   peak = fmaxf(peak, __shfl_xor_sync(0xffffffffu, peak, 2));
   x = expf(__fsub_rn(x, peak));
-  x = __fadd_rn(__fmul_rn(x, recip(sum4(x, 1))), eps);
+  x = __fadd_rn(__fmul_rn(x, rcp_fast(sum4(x, 1))), eps);
   for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) x = __fmul_rn(x, recip(__fadd_rn(sum4(x, 1), eps)));
-    x = __fmul_rn(x, recip(__fadd_rn(sum4(x, HC), eps)));
+    if (it > 0) x = __fmul_rn(x, rcp_fast(__fadd_rn(sum4(x, 1), eps)));
+    x = __fmul_rn(x, rcp_fast(__fadd_rn(sum4(x, HC), eps)));
   }
   if (live) p.comb_out[(size_t)t * LANES + e] = x;
 }
