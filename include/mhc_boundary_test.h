@@ -16,9 +16,10 @@
 extern "C" {
 #endif
 
-/* With on != 0, the tensor-core stage kernels launched from now on, on the
- * current device, issue no input copies: their waits for those copies run
- * out (after about a second) and they report MHC_ERR_TIMEOUT.  on == 0
+/* With on != 0, the tensor-core stage kernels and the one-kernel path for a
+ * few tokens launched from now on, on the current device, issue no input
+ * copies: their waits for those copies run out (after about a second) and
+ * they report MHC_ERR_TIMEOUT.  on == 0
  * restores normal operation.  Affects every handle on the device; call it
  * only while no boundary call is in flight.  Returns MHC_ERR_CUDA if the
  * device flag cannot be set. */

@@ -21,7 +21,7 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmhc_boundary.so")
 
 SOURCES = ["api.cu", "k_stage.cu", "k_stage_tc.cu", "k_finish.cu", "k_mixes.cu", "k_moe_fold.cu", "k_owner_reduce.cu",
-           "static_entry.cu"]
+           "static_entry.cu", "k_small.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

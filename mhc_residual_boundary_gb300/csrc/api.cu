@@ -45,6 +45,10 @@ struct mhc_boundary {
   float *part = nullptr;         // [cap][part_row_floats(slices)] stage-kernel partial sums
   uint16_t *fold = nullptr;      // [cap][H] bf16 stage-1 sum of MoE calls (top_k > 0) or owner sums
   unsigned int *err = nullptr;   // device-detected argument errors
+  // the one-kernel path for a few tokens (k_small.cu): CTAs a cluster (0: not
+  // available at this shape) and clusters that run at once
+  int small_cs = 0;
+  int small_clusters = 0;
   unsigned char *staging = nullptr;
   size_t staging_bytes = 0;
   // profiling: 6 events per recorded call (stage, finish, mixes: start/end)
@@ -213,6 +217,18 @@ bool side_join_needed(const mhc_boundary *b, unsigned long long capture) {
   return capture == 0 ? b->side_capture == 0 : b->side_capture == capture;
 }
 
+// Clusters the one-kernel path runs a call of m tokens on (with `tp`
+// partials a token after any fold or owner reduce), or 0 for the stage and
+// finish kernels: the FP32 weight, and every token's cluster share within the
+// tokens a cluster takes at this shape, all clusters running at once.
+int small_clusters_for(const mhc_boundary *b, int m, int tp, bool fp32_weight) {
+  if (!fp32_weight || b->small_cs == 0 || m > SMALL_M_MAX) return 0;
+  const int b_max = small_tokens_max(b->cfg.hidden, tp, b->small_cs);
+  const int clusters = m < b->small_clusters ? m : b->small_clusters;
+  if (b_max < 1 || clusters < 1 || (m + clusters - 1) / clusters > b_max) return 0;
+  return clusters;
+}
+
 mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe_args_t *moe,
                          cudaStream_t stream) {
   const mhc_boundary_config_t &c = b->cfg;
@@ -258,60 +274,103 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     sp.tp = 1;
     sp.partials = b->fold;
   }
-  // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
-  // groups (tensor-core kernel); the scratch holds the larger count
-  const bool tc_path = sp.tp <= TP_TMA_MAX;
-  sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
-  sp.residual = static_cast<const uint16_t *>(a->residual);
-  sp.post = a->post;
-  sp.comb = a->comb;
-  sp.hc_fn = a->hc_fn;
-  sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
-  sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
-  sp.early_weight = (c.flags & MHC_FLAG_STATIC_WEIGHT) != 0;
-  sp.residual_out = static_cast<uint16_t *>(a->residual_out);
-  sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
-  sp.part = b->part;
-  sp.part_stride = part_row_floats(sp.slices);
-  sp.err = b->err;
-  e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, stream);
-  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
-  if (ev) {
-    cudaEventRecord(ev[1], stream);
-    cudaEventRecord(ev[2], stream);
-  }
-
-  FinishParams fp = {};
-  fp.m = a->m;
-  fp.hidden = c.hidden;
-  fp.slices = sp.slices;
-  fp.part = b->part;
-  fp.part_stride = sp.part_stride;
-  fp.err = b->err;
-  fp.scale = a->scale;
-  fp.base = a->base;
-  fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
-  fp.streams = static_cast<const uint16_t *>(a->residual_out);
-  fp.rms_eps = c.rms_eps;
-  fp.hc_eps = c.hc_eps;
-  fp.norm_eps = c.norm_eps;
-  // post / Sinkhorn: in the finish kernel (default), or a separate kernel on
-  // the side stream ([GLM] design) or on the caller's stream
+  // post / Sinkhorn: in the boundary's own kernels (default), or a separate
+  // kernel on the side stream ([GLM] design) or on the caller's stream
   const bool separate = (c.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) != 0;
   const bool on_side = separate && !sync_mixes;
-  fp.mixes = separate ? b->mixes : nullptr;
-  fp.mixes_out = a->mixes_out;
-  fp.pre_out = a->pre_out;
-  fp.post_out = separate ? nullptr : a->post_out;
-  fp.comb_out = separate ? nullptr : a->comb_out;
-  fp.post_mult = c.post_mult;
-  fp.repeat = c.sinkhorn_repeat;
-  fp.layer_input = static_cast<uint16_t *>(a->layer_input);
-  fp.mx_values = a->mxfp8_values;
-  fp.mx_scales = a->mxfp8_scales;
-  e = launch_finish(fp, b->sm_count, stream, ev == nullptr);
-  if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
-  if (ev) cudaEventRecord(ev[3], stream);
+  // a few tokens: the whole boundary in one kernel of CTA clusters
+  const int clusters = small_clusters_for(b, a->m, sp.tp, a->hc_fn != nullptr);
+  if (clusters > 0) {
+    SmallParams q = {};
+    q.m = a->m;
+    q.hidden = c.hidden;
+    q.tp = sp.tp;
+    q.cs = b->small_cs;
+    q.cols_max = small_cols_max(c.hidden, b->small_cs);
+    q.partials = sp.partials;
+    q.residual = static_cast<const uint16_t *>(a->residual);
+    q.post = a->post;
+    q.comb = a->comb;
+    q.hc_fn = a->hc_fn;
+    q.scale = a->scale;
+    q.base = a->base;
+    q.gamma = static_cast<const uint16_t *>(a->norm_weight);
+    q.early_weight = (c.flags & MHC_FLAG_STATIC_WEIGHT) != 0;
+    q.rms_eps = c.rms_eps;
+    q.hc_eps = c.hc_eps;
+    q.norm_eps = c.norm_eps;
+    q.post_mult = c.post_mult;
+    q.repeat = c.sinkhorn_repeat;
+    q.residual_out = static_cast<uint16_t *>(a->residual_out);
+    q.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+    q.layer_input = static_cast<uint16_t *>(a->layer_input);
+    q.mixes = separate ? b->mixes : nullptr;
+    q.mixes_out = a->mixes_out;
+    q.pre_out = a->pre_out;
+    q.post_out = separate ? nullptr : a->post_out;
+    q.comb_out = separate ? nullptr : a->comb_out;
+    q.mx_values = a->mxfp8_values;
+    q.mx_scales = a->mxfp8_scales;
+    q.err = b->err;
+    e = launch_small(q, clusters, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "boundary kernel: %s", cudaGetErrorString(e));
+    if (ev) {
+      cudaEventRecord(ev[1], stream);
+      cudaEventRecord(ev[2], stream);
+      cudaEventRecord(ev[3], stream);
+    }
+  } else {
+    // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
+    // groups (tensor-core kernel); the scratch holds the larger count
+    const bool tc_path = sp.tp <= TP_TMA_MAX;
+    sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
+    sp.residual = static_cast<const uint16_t *>(a->residual);
+    sp.post = a->post;
+    sp.comb = a->comb;
+    sp.hc_fn = a->hc_fn;
+    sp.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
+    sp.fn_terms = a->hc_fn_bf16 ? 1 : 3;
+    sp.early_weight = (c.flags & MHC_FLAG_STATIC_WEIGHT) != 0;
+    sp.residual_out = static_cast<uint16_t *>(a->residual_out);
+    sp.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+    sp.part = b->part;
+    sp.part_stride = part_row_floats(sp.slices);
+    sp.err = b->err;
+    e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
+    if (ev) {
+      cudaEventRecord(ev[1], stream);
+      cudaEventRecord(ev[2], stream);
+    }
+
+    FinishParams fp = {};
+    fp.m = a->m;
+    fp.hidden = c.hidden;
+    fp.slices = sp.slices;
+    fp.part = b->part;
+    fp.part_stride = sp.part_stride;
+    fp.err = b->err;
+    fp.scale = a->scale;
+    fp.base = a->base;
+    fp.gamma = static_cast<const uint16_t *>(a->norm_weight);
+    fp.streams = static_cast<const uint16_t *>(a->residual_out);
+    fp.rms_eps = c.rms_eps;
+    fp.hc_eps = c.hc_eps;
+    fp.norm_eps = c.norm_eps;
+    fp.mixes = separate ? b->mixes : nullptr;
+    fp.mixes_out = a->mixes_out;
+    fp.pre_out = a->pre_out;
+    fp.post_out = separate ? nullptr : a->post_out;
+    fp.comb_out = separate ? nullptr : a->comb_out;
+    fp.post_mult = c.post_mult;
+    fp.repeat = c.sinkhorn_repeat;
+    fp.layer_input = static_cast<uint16_t *>(a->layer_input);
+    fp.mx_values = a->mxfp8_values;
+    fp.mx_scales = a->mxfp8_scales;
+    e = launch_finish(fp, b->sm_count, stream, ev == nullptr);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
+    if (ev) cudaEventRecord(ev[3], stream);
+  }
 
   if (separate) {
     MixesParams mp = {};
@@ -515,7 +574,21 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   cudaError_t e = stage_set_attributes();
   if (e == cudaSuccess) e = stage_tc_set_attributes();
   if (e == cudaSuccess) e = finish_set_attributes();
+  if (e == cudaSuccess) e = small_set_attributes();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b->sm_count, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess) {
+    // the one-kernel path: 16-CTA clusters where they fit at this shape, else 8
+    for (int cs : {16, 8}) {
+      const int b_max = small_tokens_max(c.hidden, c.tp, cs);
+      if (b_max < 1) continue;
+      const int n = small_active_clusters(cs, small_smem_bytes(c.hidden, c.tp, cs, b_max));
+      if (n >= 1) {
+        b->small_cs = cs;
+        b->small_clusters = n;
+        break;
+      }
+    }
+  }
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->side, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->main_ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->side_done, cudaEventDisableTiming);
@@ -699,8 +772,13 @@ size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden) { return scale_bytes(m, 
 
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) {
   if (!b) return 0;
-  return ((b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 3 : 2) +
-         ((b->cfg.flags & MHC_FLAG_OWNER_REDUCE) ? 1 : 0);
+  // for a call of max_num_tokens tokens with the FP32 weight: the one-kernel
+  // path, or the stage and finish kernels; plus a separate post / Sinkhorn
+  // kernel, plus the owner reduce
+  const bool owner = (b->cfg.flags & MHC_FLAG_OWNER_REDUCE) != 0;
+  const int tp = owner ? 1 : b->cfg.tp;
+  const int core = small_clusters_for(b, b->cfg.max_num_tokens, tp, true) > 0 ? 1 : 2;
+  return core + ((b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 1 : 0) + (owner ? 1 : 0);
 }
 
 mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls) {
@@ -763,6 +841,7 @@ const char *mhc_last_error(const mhc_boundary_t *b) {
 }  // extern "C"
 
 mhc_status_t mhc_test_stall_stage_copies(int32_t on) {
-  const cudaError_t e = stage_tc_stall_copies(on ? 1 : 0);
+  cudaError_t e = stage_tc_stall_copies(on ? 1 : 0);
+  if (e == cudaSuccess) e = small_stall_copies(on ? 1 : 0);
   return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA;
 }

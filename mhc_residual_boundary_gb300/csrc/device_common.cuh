@@ -205,4 +205,88 @@ static __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, co
   for (int i = 0; i < HC * HC; ++i) dst[i] = c[i];
 }
 
+// Paired four-term sum over the lanes that differ in bits a and 2a.
+__device__ __forceinline__ float lane_sum4(float x, int a) {
+  const float s = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, a));
+  return __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2 * a));
+}
+
+// The same post-mix and Sinkhorn mix with a token spread over 16 lanes, one
+// matrix element each (lane 4r + k of the token's half-warp; the whole warp
+// calls it, a half-warp per token): a row sum is two butterfly shuffles over
+// lanes 4r .. 4r+3 (xor 1 then xor 2 gives (c0 + c1) + (c2 + c3) on every
+// lane of the row), a column sum two over lanes k, k+4, k+8, k+12 (xor 4
+// then xor 8); lanes 0-3 of the token also compute post.  The operations are
+// those of post_and_sinkhorn, so the bits are the same.  `mix` points at the
+// token's 24 normalised mixes; half-warps with live == false compute on zeros
+// and store nothing.
+__device__ __forceinline__ void post_and_sinkhorn16(const MixArgs p, int t, const float *mix, bool live) {
+  const int e = threadIdx.x & (HC * HC - 1);
+  if (live && e < HC) {
+    const float z = __fadd_rn(__fmul_rn(mix[HC + e], p.scale[1]), p.base[HC + e]);
+    p.post_out[(size_t)t * HC + e] = __fmul_rn(sigmoid(z), p.post_mult);
+  }
+  const float eps = p.eps;
+  float x = live ? __fadd_rn(__fmul_rn(mix[2 * HC + e], p.scale[2]), p.base[2 * HC + e]) : 0.f;
+  // row softmax
+  float peak = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  peak = fmaxf(peak, __shfl_xor_sync(0xffffffffu, peak, 2));
+  x = expf(__fsub_rn(x, peak));
+  x = __fadd_rn(__fmul_rn(x, rcp_fast(lane_sum4(x, 1))), eps);
+  for (int it = 0; it < p.repeat; ++it) {
+    if (it > 0) x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, 1), eps)));
+    x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, HC), eps)));
+  }
+  if (live) p.comb_out[(size_t)t * HC * HC + e] = x;
+}
+
+// The same post-mix and Sinkhorn mix with a token spread over 4 lanes, one
+// matrix row each (lane r of the token's quad): a row sum is the paired sum
+// in registers, a column sum two butterfly shuffles over the quad (xor 1
+// then xor 2 gives (c0k + c1k) + (c2k + c3k) on every lane), the four
+// columns' chains side by side; lane r also computes post_r.  The
+// operations are those of post_and_sinkhorn, so the bits are the same.  The
+// whole warp calls it, a quad per token; quads with live == false compute on
+// zeros and store nothing.
+__device__ __forceinline__ void post_and_sinkhorn4(const MixArgs p, int t, const float *mix, bool live) {
+  const int r = threadIdx.x & (HC - 1);
+  if (live) {
+    const float z = __fadd_rn(__fmul_rn(mix[HC + r], p.scale[1]), p.base[HC + r]);
+    p.post_out[(size_t)t * HC + r] = __fmul_rn(sigmoid(z), p.post_mult);
+  }
+  const float eps = p.eps, s2 = p.scale[2];
+  float c[HC];
+#pragma unroll
+  for (int k = 0; k < HC; ++k)
+    c[k] = live ? __fadd_rn(__fmul_rn(mix[2 * HC + HC * r + k], s2), p.base[2 * HC + HC * r + k]) : 0.f;
+  {
+    const float peak = fmaxf(fmaxf(c[0], c[1]), fmaxf(c[2], c[3]));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) c[k] = expf(__fsub_rn(c[k], peak));
+    const float inv = rcp_fast(sum4_paired(c[0], c[1], c[2], c[3]));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) c[k] = __fadd_rn(__fmul_rn(c[k], inv), eps);
+  }
+#pragma unroll 1
+  for (int it = 0; it < p.repeat; ++it) {
+    if (it > 0) {
+      const float inv = rcp_fast(__fadd_rn(sum4_paired(c[0], c[1], c[2], c[3]), eps));
+#pragma unroll
+      for (int k = 0; k < HC; ++k) c[k] = __fmul_rn(c[k], inv);
+    }
+    float s[HC];
+#pragma unroll
+    for (int k = 0; k < HC; ++k) s[k] = __fadd_rn(c[k], __shfl_xor_sync(0xffffffffu, c[k], 1));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xffffffffu, s[k], 2));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) c[k] = __fmul_rn(c[k], rcp_fast(__fadd_rn(s[k], eps)));
+  }
+  if (live) {
+    float *dst = p.comb_out + (size_t)t * HC * HC + HC * r;
+#pragma unroll
+    for (int k = 0; k < HC; ++k) dst[k] = c[k];
+  }
+}
+
 }  // namespace mhc

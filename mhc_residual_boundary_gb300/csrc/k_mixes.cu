@@ -28,34 +28,12 @@ constexpr int NT = 128;
 constexpr int LANES = HC * HC;             // lanes per token
 constexpr int TOKENS = NT / LANES;         // tokens per CTA
 
-// Paired four-term sum over the lanes that differ in bits a and 2a.
-__device__ __forceinline__ float sum4(float x, int a) {
-  const float s = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, a));
-  return __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, 2 * a));
-}
-
 __global__ void __launch_bounds__(NT) k_mixes(const MixesParams p) {
-  const int e = threadIdx.x & (LANES - 1);        // element 4r + k
   const int t = blockIdx.x * TOKENS + threadIdx.x / LANES;
   // the whole warp runs the shuffles; lanes of a token past m compute on zeros
   const bool live = t < p.m;
-  const float *row = p.mixes + (size_t)(live ? t : 0) * MIX;
-  if (live && e < HC) {
-    const float z = __fadd_rn(__fmul_rn(row[HC + e], p.scale[1]), p.base[HC + e]);
-    p.post_out[(size_t)t * HC + e] = __fmul_rn(sigmoid(z), p.post_mult);
-  }
-  const float eps = p.eps;
-  float x = live ? __fadd_rn(__fmul_rn(row[2 * HC + e], p.scale[2]), p.base[2 * HC + e]) : 0.f;
-  // row softmax
-  float peak = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
-  peak = fmaxf(peak, __shfl_xor_sync(0xffffffffu, peak, 2));
-  x = expf(__fsub_rn(x, peak));
-  x = __fadd_rn(__fmul_rn(x, rcp_fast(sum4(x, 1))), eps);
-  for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) x = __fmul_rn(x, rcp_fast(__fadd_rn(sum4(x, 1), eps)));
-    x = __fmul_rn(x, rcp_fast(__fadd_rn(sum4(x, HC), eps)));
-  }
-  if (live) p.comb_out[(size_t)t * LANES + e] = x;
+  const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.eps, p.repeat};
+  post_and_sinkhorn16(ma, t, p.mixes + (size_t)(live ? t : 0) * MIX, live);
 }
 
 }  // namespace

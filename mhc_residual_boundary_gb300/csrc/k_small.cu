@@ -1,0 +1,569 @@
+// k_small.cu -- the whole boundary of a few tokens in one kernel.
+//
+// A cluster of CS CTAs (16, or 8 where 16 do not fit) owns up to B_MAX tokens
+// and every CTA of it one contiguous range of the hidden columns (whole
+// 32-column blocks when H is a multiple of 32), as the pages lay out their
+// boundary kernels ([GLM] _BoundaryDeviceKernel.kernel: one token per CTA
+// cluster, the 24-way GEMV summed over the cluster through distributed shared
+// memory).  Per CTA, in one pass:
+//   1. bulk copies bring the CTA's prenorm weight rows (FP32, [4][cols][24];
+//      for a layer weight before the wait for the preceding kernel) and each
+//      token's partials, streams, post and comb for its columns;
+//   2. stage-1 sum of the tp partials in FP32 in rank order, rounded to BF16
+//      ([DSV] _LamportMHCDeviceKernel.kernel, lane_sum), post-mix of the four
+//      streams ([GLM] "mixed"), with the operations of the tensor-core stage
+//      kernel (so the same bits); residual_out stored, the new streams kept in
+//      shared memory;
+//   3. the CTA's part of the GEMV and the sum of squares ([GLM] "partial"):
+//      FP32 fused multiply-adds of the BF16 streams (exact as FP32) with the
+//      FP32 weight, split over threads by (4 outputs, row phase) with every
+//      token of the cluster in each thread (the weight is read once), summed
+//      back in a fixed shuffle tree;
+//   4. cluster barrier; every CTA sums the CS partials of each token in rank
+//      order from the other CTAs' shared memory, then rstd, mixes and pre
+//      ([GLM] "rstd", "pre_mix") -- the same values in every CTA;
+//   5. collapse c = bf16((n0 p0 + n1 p1) + (n2 p2 + n3 p3)) of its columns
+//      and their sum of c^2; cluster barrier; inv_rms from the CS sums in rank
+//      order; out = bf16((c * inv_rms) * gamma) and the optional MXFP8 copy
+//      ([GLM] "collapse", "inv_rms"; [DSV] quantize branch);
+//   6. token t's post and Sinkhorn mix ([GLM] _MixesDeviceKernel) in four
+//      lanes of CTA rank t % CS's last warp (the same operations as the
+//      finish kernel's, so the same bits), from right after step 4, while
+//      the other warps collapse and normalise.
+// A last cluster barrier keeps every CTA's shared memory alive until the
+// others have read it.  The copy waits are bounded; a CTA whose copies do not
+// arrive skips its work (its outputs are invalid), still takes part in every
+// cluster barrier, and sets bit 1 of the error word.
+//
+// Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
+//        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
+#include "device_common.cuh"
+#include "launch.cuh"
+#include "tcgen05.cuh"
+
+namespace mhc {
+namespace {
+
+// Test hook (mhc_test_stall_stage_copies): when set, no token data copies are
+// issued, so the kernel's bounded wait runs out and it reports the timeout
+// through the error word instead of hanging.
+__device__ int g_stall_copies = 0;
+
+constexpr int NT = 512;
+constexpr int NWARP = NT / 32;
+constexpr int SINK_WARP = NWARP - 1;           // post / Sinkhorn, no collapse items
+constexpr int ITEM_THREADS = NT - 32;          // threads of the collapse and normalisation items
+constexpr int GEMV_ROWS_WARP = 5;              // weight rows a warp takes at once (30 lanes)
+constexpr int GEMV_ROWS_PASS = GEMV_ROWS_WARP * NWARP;   // 80
+constexpr uint32_t WAIT_LIMIT = 1u << 22;      // polls before a copy wait gives up
+constexpr int SMEM_MAX = 227 * 1024;
+
+// Shared memory: control block, then the weight rows, then one slot per token.
+struct Ctl {
+  static constexpr int wbar = 0;               // uint64: weight rows arrived
+  static constexpr int dbar = 8;               // uint64: token data arrived
+  static constexpr int red = 16;               // f32 [SMALL_B_MAX][25]: GEMV partials + sum of squares
+  static constexpr int red2 = red + SMALL_B_MAX * VALUES * 4;   // f32 [SMALL_B_MAX]: sum of c^2
+  static constexpr int pre = red2 + SMALL_B_MAX * 4;             // f32 [SMALL_B_MAX][4]
+  static constexpr int ir = pre + SMALL_B_MAX * 16;              // f32 [SMALL_B_MAX]
+  static constexpr int mix = ir + SMALL_B_MAX * 4;               // f32 [SMALL_B_MAX][24]
+  static constexpr int item_ss = mix + SMALL_B_MAX * MIX * 4;    // f32 [SMALL_ITEMS_MAX]
+  static constexpr int gred = item_ss + SMALL_ITEMS_MAX * 4;     // f32 [16 warps][SMALL_B_MAX][24]: the warps' GEMV sums
+  static constexpr int bad = gred + NWARP * SMALL_B_MAX * MIX * 4; // int: a copy wait gave up
+  static constexpr int end = (bad + 4 + 127) / 128 * 128;
+};
+
+__host__ __device__ constexpr int weight_bytes(int cols) { return HC * cols * MIX * 4; }
+// A token's slot: partials [tp][cols] bf16, streams [4][cols] bf16, post [4]
+// and comb [16] f32.
+__host__ __device__ constexpr int slot_res(int tp, int cols) { return tp * cols * 2; }
+__host__ __device__ constexpr int slot_post(int tp, int cols) { return slot_res(tp, cols) + HC * cols * 2; }
+__host__ __device__ constexpr int slot_bytes(int tp, int cols) { return (slot_post(tp, cols) + 80 + 127) / 128 * 128; }
+
+// Column range of cluster rank r (whole units of `unit` columns).
+__device__ __forceinline__ void col_range(int hidden, int cs, int r, int &c0, int &c1) {
+  const int unit = hidden % 32 == 0 ? 32 : VEC, n = hidden / unit;
+  c0 = int((long long)r * n / cs) * unit;
+  c1 = int((long long)(r + 1) * n / cs) * unit;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster: arrive (release), then wait (acquire).
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+// A float of cluster CTA `rank`'s shared memory at this CTA's address `p`.
+__device__ __forceinline__ float ld_cluster(const void *p, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// The 15 warps other than the post / Sinkhorn warp.
+__device__ __forceinline__ void item_sync() { asm volatile("bar.sync 1, %0;" ::"n"(ITEM_THREADS) : "memory"); }
+
+// Sum over the 32 lanes of a warp in a fixed tree (every lane gets it).
+__device__ __forceinline__ float tree_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float lane4(const float4 &v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+struct GemvArgs {
+  const float *w;              // the weight rows [4 * cols][24]
+  const unsigned char *x;      // token 0's new streams [4][cols] bf16; token t at + t * sbytes
+  int sbytes, K;               // K = 4 * cols rows
+  float *gred;                 // [16 warps][SMALL_B_MAX][24]: each warp's sums
+};
+
+// This CTA's part of the GEMV for B tokens: lane l < 30 of warp w takes
+// outputs 4 * (l % 6) .. +3 of rows k = 5 * w + l / 6, + 80, + 160, ... (a warp
+// reads 5 whole 96-byte weight rows, without bank conflicts); each warp's
+// five row lanes of an output quad are summed in order into gred.
+template <int B>
+__device__ __noinline__ void gemv_part(const GemvArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int iq = lane % 6, rr = lane / 6;
+  float4 acc[B];
+#pragma unroll
+  for (int t = 0; t < B; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane < 30) {
+    const float *w = a.w + iq * 4;
+    for (int k = GEMV_ROWS_WARP * warp + rr; k < a.K; k += GEMV_ROWS_PASS) {
+      const float4 wv = *reinterpret_cast<const float4 *>(w + k * MIX);
+#pragma unroll
+      for (int t = 0; t < B; ++t) {
+        const float x = __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t *>(a.x + t * a.sbytes + k * 2)) << 16);
+        acc[t].x = fmaf(wv.x, x, acc[t].x);
+        acc[t].y = fmaf(wv.y, x, acc[t].y);
+        acc[t].z = fmaf(wv.z, x, acc[t].z);
+        acc[t].w = fmaf(wv.w, x, acc[t].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < B; ++t) {
+    float4 v = acc[t];
+#pragma unroll
+    for (int r = 1; r < GEMV_ROWS_WARP; ++r) {
+      const int src = (lane + 6 * r) & 31;
+      v.x = __fadd_rn(v.x, __shfl_sync(0xffffffffu, acc[t].x, src));
+      v.y = __fadd_rn(v.y, __shfl_sync(0xffffffffu, acc[t].y, src));
+      v.z = __fadd_rn(v.z, __shfl_sync(0xffffffffu, acc[t].z, src));
+      v.w = __fadd_rn(v.w, __shfl_sync(0xffffffffu, acc[t].w, src));
+    }
+    if (lane < 6) *reinterpret_cast<float4 *>(a.gred + ((warp * SMALL_B_MAX) + t) * MIX + lane * 4) = v;
+  }
+}
+
+__global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Ctl::wbar);
+  uint64_t *dbar = reinterpret_cast<uint64_t *>(smem + Ctl::dbar);
+  float *red = reinterpret_cast<float *>(smem + Ctl::red);
+  float *red2 = reinterpret_cast<float *>(smem + Ctl::red2);
+  float *pre_s = reinterpret_cast<float *>(smem + Ctl::pre);
+  float *ir_s = reinterpret_cast<float *>(smem + Ctl::ir);
+  float *mix_s = reinterpret_cast<float *>(smem + Ctl::mix);
+  float *item_ss = reinterpret_cast<float *>(smem + Ctl::item_ss);
+  volatile int *bad = reinterpret_cast<volatile int *>(smem + Ctl::bad);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = p.hidden, tp = p.tp, cs = p.cs;
+  const uint32_t rank = cluster_rank();
+  const int cluster = int(blockIdx.x) / cs;
+  // tokens of this cluster: [t0, t1)
+  const int n_clusters = int(gridDim.x) / cs;
+  const int t0 = int((long long)cluster * p.m / n_clusters), t1 = int((long long)(cluster + 1) * p.m / n_clusters);
+  const int b = t1 - t0;
+  int c0, c1;
+  col_range(H, cs, int(rank), c0, c1);
+  const int cols = c1 - c0, F = cols / VEC;           // 16-byte fragments of a row piece
+  unsigned char *w_s = smem + Ctl::end;
+  unsigned char *slots = w_s + weight_bytes(p.cols_max);
+  const int sbytes = slot_bytes(tp, p.cols_max);
+
+  if (tid == 0) {
+    tc::mbar_init(wbar, 1);
+    tc::mbar_init(dbar, 1);
+    *bad = 0;
+    tc::mbar_init_fence();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  // the weight rows of this CTA's columns (a layer weight: before the wait)
+  auto load_weight = [&]() {
+    if (warp == 0 && cols > 0) {
+      if (lane == 0) tc::mbar_arrive_expect_tx(wbar, uint32_t(weight_bytes(cols)));
+      __syncwarp();
+      if (lane < HC)
+        tc::bulk_load(w_s + lane * cols * MIX * 4, p.hc_fn + ((size_t)lane * H + c0) * MIX, uint32_t(cols * MIX * 4), wbar);
+    }
+  };
+  if (p.early_weight) load_weight();
+  pdl_wait();
+  if (!p.early_weight) load_weight();
+  // each token's partials, streams, post and comb (lanes of warp 0 issue)
+  const bool stall = *static_cast<volatile int *>(&g_stall_copies) != 0;
+  if (warp == 0 && b > 0 && !stall) {
+    const uint32_t per_token = uint32_t((tp + HC) * cols * 2 + 80);
+    if (lane == 0) tc::mbar_arrive_expect_tx(dbar, cols > 0 ? per_token * uint32_t(b) : uint32_t(b) * 80u);
+    __syncwarp();
+    const int per = tp + HC + 2;
+    for (int e = lane; e < b * per; e += 32) {
+      const int tl = e / per, k = e % per, t = t0 + tl;
+      unsigned char *st = slots + tl * sbytes;
+      if (k < tp) {
+        if (cols > 0) tc::bulk_load(st + k * cols * 2, p.partials + ((size_t)k * p.m + t) * H + c0, uint32_t(cols * 2), dbar);
+      } else if (k < tp + HC) {
+        const int j = k - tp;
+        if (cols > 0)
+          tc::bulk_load(st + slot_res(tp, cols) + j * cols * 2, p.residual + ((size_t)t * HC + j) * H + c0,
+                        uint32_t(cols * 2), dbar);
+      } else if (k == tp + HC) {
+        tc::bulk_load(st + slot_post(tp, cols), p.post + (size_t)t * HC, 16u, dbar);
+      } else {
+        tc::bulk_load(st + slot_post(tp, cols) + 16, p.comb + (size_t)t * HC * HC, 64u, dbar);
+      }
+    }
+  }
+  if (b > 0 && !tc::mbar_wait_bounded(dbar, 0u, WAIT_LIMIT)) *bad = 1;
+  if (b > 0 && cols > 0 && !tc::mbar_wait_bounded(wbar, 0u, WAIT_LIMIT)) *bad = 1;
+  __syncthreads();
+  const bool ok = *bad == 0;
+
+  // ---- 2. stage-1 sum and post-mix: item (token, fragment)
+  const int n_items = b * F;
+  for (int item = tid; ok && item < n_items; item += NT) {
+    const int tl = item / F, f = item % F, t = t0 + tl;
+    unsigned char *st = slots + tl * sbytes;
+    float2 y[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
+    for (int r = 0; r < tp; ++r) {
+      const uint4 w = *reinterpret_cast<const uint4 *>(st + r * cols * 2 + f * 16);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        y[e].x = __fadd_rn(y[e].x, bf16_lo(ww[e]));
+        y[e].y = __fadd_rn(y[e].y, bf16_hi(ww[e]));
+      }
+    }
+    const uint4 yb = make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
+                                pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
+    const uint32_t ybw[4] = {yb.x, yb.y, yb.z, yb.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = bf16_pair(ybw[e]);
+    if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * H + c0 + f * VEC, yb);
+    unsigned char *rs = st + slot_res(tp, cols) + f * 16;
+    uint4 res[HC];
+#pragma unroll
+    for (int k = 0; k < HC; ++k) res[k] = *reinterpret_cast<const uint4 *>(rs + k * cols * 2);
+    const float4 post = *reinterpret_cast<const float4 *>(st + slot_post(tp, cols));
+    float4 comb[HC];
+#pragma unroll
+    for (int k = 0; k < HC; ++k) comb[k] = *reinterpret_cast<const float4 *>(st + slot_post(tp, cols) + 16 + k * 16);
+    float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+      const float2 pj = dup(lane4(post, j));
+      float2 o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = __fmul2_rn(y[e], pj);
+#pragma unroll
+      for (int k = 0; k < HC; ++k) {
+        const float2 ck = dup(lane4(comb[k], j));
+        const uint32_t ww[4] = {res[k].x, res[k].y, res[k].z, res[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = __ffma2_rn(bf16_pair(ww[e]), ck, o[e]);
+      }
+      const uint4 nv = make_uint4(pack_bf16x2(o[0].x, o[0].y), pack_bf16x2(o[1].x, o[1].y),
+                                  pack_bf16x2(o[2].x, o[2].y), pack_bf16x2(o[3].x, o[3].y));
+      const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 r2 = bf16_pair(nw[e]);
+        ss2 = __ffma2_rn(r2, r2, ss2);
+      }
+      // the new stream replaces the source stream in the slot (each item owns
+      // its 16 bytes of every stream)
+      *reinterpret_cast<uint4 *>(rs + j * cols * 2) = nv;
+      st_vec(p.residual_out + ((size_t)t * HC + j) * H + c0 + f * VEC, nv);
+    }
+    item_ss[item] = __fadd_rn(ss2.x, ss2.y);
+  }
+  __syncthreads();
+
+  // ---- 3. this CTA's part of the GEMV (gemv_part: the loop over the
+  // cluster's tokens unrolled for their number)
+  float *gred = reinterpret_cast<float *>(smem + Ctl::gred);
+  {
+    const GemvArgs ga = {reinterpret_cast<const float *>(w_s), slots + slot_res(tp, cols), sbytes, HC * cols, gred};
+    switch (ok ? b : 0) {
+      case 1: gemv_part<1>(ga); break;
+      case 2: gemv_part<2>(ga); break;
+      case 3: gemv_part<3>(ga); break;
+      case 4: gemv_part<4>(ga); break;
+      case 5: gemv_part<5>(ga); break;
+      case 6: gemv_part<6>(ga); break;
+      case 7: gemv_part<7>(ga); break;
+      case 8: gemv_part<8>(ga); break;
+      default: break;
+    }
+  }
+  // the sum of squares of token `warp`'s new streams, over its fragments in
+  // a fixed tree
+  if (warp < b) {
+    float s = 0.f;
+    for (int f = lane; f < F; f += 32) s = __fadd_rn(s, ok ? item_ss[warp * F + f] : 0.f);
+    s = tree_sum(s);
+    if (lane == 0) red[warp * VALUES + MIX] = s;
+  }
+  __syncthreads();
+  // the 16 warps' sums of output i of token t, in warp order
+  if (tid < b * MIX) {
+    const int t = tid / MIX, i = tid % MIX;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) v = __fadd_rn(v, gred[((w * SMALL_B_MAX) + t) * MIX + i]);
+    red[t * VALUES + i] = v;
+  }
+  // ---- 4. the cluster's sums, rank order; rstd, mixes, pre
+  cluster_sync();
+  if (warp < b) {
+    // the cs partials first (independent loads), then their sum in rank order
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) x[r] = lane < VALUES && r < cs ? ld_cluster(red + warp * VALUES + lane, uint32_t(r)) : 0.f;
+    float v = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < cs) v = __fadd_rn(v, x[r]);
+    const int t = t0 + warp;
+    const float ss = __shfl_sync(0xffffffffu, v, MIX);
+    const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
+    const float mix = lane < MIX ? __fmul_rn(v, rstd) : 0.f;
+    const bool mine = int(rank) == t % cs;   // this CTA writes the token's mixes, pre, post, comb
+    if (lane < MIX) {
+      mix_s[warp * MIX + lane] = mix;
+      if (mine && p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
+      if (mine && p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
+    }
+    if (lane < HC) {
+      const float pr = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+      pre_s[warp * HC + lane] = pr;
+      if (mine && p.pre_out) p.pre_out[(size_t)t * HC + lane] = pr;
+    }
+  }
+  __syncthreads();
+
+  // ---- 5. collapse of this CTA's columns (kept in registers for step 7);
+  // meanwhile the last warp runs post and the Sinkhorn mix of this CTA's
+  // tokens (it has no items and arrives at the next cluster barrier early)
+  constexpr int IPT = (SMALL_ITEMS_MAX + ITEM_THREADS - 1) / ITEM_THREADS;   // items a thread
+  uint32_t cw[IPT][4];
+  if (warp == SINK_WARP) {
+    cluster_arrive();
+    if (p.post_out) {
+      // tokens t of this cluster with t % cs == rank, one a quad of lanes
+      const int first = (int(rank) - t0 % cs + cs) % cs;   // first local index with (t0 + i) % cs == rank
+      const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
+      for (int i0 = first; i0 < b; i0 += 8 * cs) {
+        const int i = i0 + (lane >> 2) * cs;
+        const bool live = ok && i < b;
+        post_and_sinkhorn4(ma, t0 + (live ? i : 0), mix_s + (live ? i : 0) * MIX, live);
+      }
+    }
+    cluster_wait();
+  } else {
+#pragma unroll
+    for (int n = 0; n < IPT; ++n) {
+      const int item = tid + n * ITEM_THREADS;
+      float s = 0.f;
+      if (ok && item < n_items) {
+        const int tl = item / F, f = item % F;
+        const unsigned char *rs = slots + tl * sbytes + slot_res(tp, cols) + f * 16;
+        const float4 pr = *reinterpret_cast<const float4 *>(pre_s + tl * HC);
+        const uint4 w0 = *reinterpret_cast<const uint4 *>(rs), w1 = *reinterpret_cast<const uint4 *>(rs + cols * 2);
+        const uint4 w2 = *reinterpret_cast<const uint4 *>(rs + 2 * cols * 2);
+        const uint4 w3 = *reinterpret_cast<const uint4 *>(rs + 3 * cols * 2);
+        const uint32_t n0[4] = {w0.x, w0.y, w0.z, w0.w}, n1[4] = {w1.x, w1.y, w1.z, w1.w};
+        const uint32_t n2[4] = {w2.x, w2.y, w2.z, w2.w}, n3[4] = {w3.x, w3.y, w3.z, w3.w};
+        float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 a = __fadd2_rn(__fmul2_rn(bf16_pair(n0[e]), dup(pr.x)), __fmul2_rn(bf16_pair(n1[e]), dup(pr.y)));
+          const float2 c = __fadd2_rn(__fmul2_rn(bf16_pair(n2[e]), dup(pr.z)), __fmul2_rn(bf16_pair(n3[e]), dup(pr.w)));
+          const float2 v = __fadd2_rn(a, c);
+          cw[n][e] = pack_bf16x2(v.x, v.y);
+          const float2 r2 = bf16_pair(cw[n][e]);
+          ss2 = __ffma2_rn(r2, r2, ss2);
+        }
+        s = __fadd_rn(ss2.x, ss2.y);
+      }
+      if (item < n_items) item_ss[item] = s;
+    }
+    item_sync();
+    // sum of c^2 of token `warp`, over its fragments in a fixed tree
+    if (warp < b) {
+      float s = 0.f;
+      for (int f = lane; f < F; f += 32) s = __fadd_rn(s, item_ss[warp * F + f]);
+      s = tree_sum(s);
+      if (lane == 0) red2[warp] = s;
+    }
+    // the norm-weight fragments, requested before the barrier
+    uint4 gw[IPT];
+#pragma unroll
+    for (int n = 0; n < IPT; ++n) {
+      const int item = tid + n * ITEM_THREADS;
+      gw[n] = ok && item < n_items ? ld_ro(p.gamma + c0 + (item % F) * VEC) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // ---- 6. cluster barrier
+    cluster_arrive();
+    cluster_wait();
+    // ---- 7. inv_rms of each token (the CS sums in rank order), normalisation
+    if (warp < b) {
+      const float x = lane < cs ? ld_cluster(red2 + warp, uint32_t(lane)) : 0.f;
+      float s = 0.f;
+      for (int r = 0; r < cs; ++r) s = __fadd_rn(s, __shfl_sync(0xffffffffu, x, r));
+      if (lane == 0) ir_s[warp] = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(s, float(H)), p.norm_eps)));
+    }
+    item_sync();
+    const int scols = H / 32;
+#pragma unroll
+    for (int n = 0; n < IPT; ++n) {
+      const int item = tid + n * ITEM_THREADS;
+      // items of a token are consecutive threads, so that a 32-element
+      // block is four consecutive lanes (cols and c0 are multiples of 32
+      // with MXFP8)
+      const bool live = ok && item < n_items;
+      const int tl = live ? item / F : 0, f = live ? item % F : 0, t = t0 + tl, h = c0 + f * VEC;
+      const float ir = ir_s[tl];
+      const uint32_t gv[4] = {gw[n].x, gw[n].y, gw[n].z, gw[n].w};
+      uint32_t ow[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 o = __fmul2_rn(__fmul2_rn(bf16_pair(cw[n][e]), dup(ir)), bf16_pair(gv[e]));
+        ow[e] = live ? pack_bf16x2(o.x, o.y) : 0u;
+      }
+      if (live) st_vec(p.layer_input + (size_t)t * H + h, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+      if (p.mx_values) {
+        const uint32_t m2 = bf16x2_max(bf16x2_max(ow[0] & 0x7fff7fffu, ow[1] & 0x7fff7fffu),
+                                       bf16x2_max(ow[2] & 0x7fff7fffu, ow[3] & 0x7fff7fffu));
+        float amax = fmaxf(bf16_lo(m2), bf16_hi(m2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t e8 = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
+        const float2 inv2 = dup(inv_scale(e8));
+        if (live) {
+          const float2 q0 = __fmul2_rn(bf16_pair(ow[0]), inv2), q1 = __fmul2_rn(bf16_pair(ow[1]), inv2);
+          const float2 q2 = __fmul2_rn(bf16_pair(ow[2]), inv2), q3 = __fmul2_rn(bf16_pair(ow[3]), inv2);
+          uint2 q;
+          q.x = e4m3x4(q0.x, q0.y, q1.x, q1.y);
+          q.y = e4m3x4(q2.x, q2.y, q3.x, q3.y);
+          *reinterpret_cast<uint2 *>(p.mx_values + (size_t)t * H + h) = q;
+          if ((f & 3) == 0) p.mx_scales[swizzle_128x4(t, h / 32, scols)] = uint8_t(e8);
+        }
+      }
+    }
+  }
+  // MXFP8 padding rows of the scale layout (cluster 0): scales zeroed
+  if (p.mx_scales && cluster == 0) {
+    const int padded = (p.m + 127) / 128 * 128, scols = H / 32;
+    for (int row = p.m + int(rank); row < padded; row += cs)
+      for (int c4 = tid; c4 < scols / 4; c4 += NT)
+        *reinterpret_cast<uint32_t *>(p.mx_scales + swizzle_128x4(row, c4 * 4, scols)) = 0u;
+  }
+  if (tid == 0 && !ok && p.err) atomicOr(p.err, 2u);
+  // no CTA leaves while another may still read its shared memory
+  cluster_sync();
+}
+
+}  // namespace
+
+cudaError_t small_stall_copies(int on) { return cudaMemcpyToSymbol(g_stall_copies, &on, sizeof on); }
+
+int small_cols_max(int hidden, int cs) {
+  const int unit = hidden % 32 == 0 ? 32 : VEC, n = hidden / unit;
+  return (n + cs - 1) / cs * unit;
+}
+
+size_t small_smem_bytes(int hidden, int tp, int cs, int tokens) {
+  const int cols = small_cols_max(hidden, cs);
+  return size_t(Ctl::end) + size_t(weight_bytes(cols)) + size_t(tokens) * slot_bytes(tp, cols);
+}
+
+// Tokens one cluster can take at this shape (0: the path does not apply).
+int small_tokens_max(int hidden, int tp, int cs) {
+  const int cols = small_cols_max(hidden, cs), f = cols / VEC;
+  int b = SMALL_B_MAX;
+  while (b > 0 && (small_smem_bytes(hidden, tp, cs, b) > size_t(SMEM_MAX) || b * f > SMALL_ITEMS_MAX)) --b;
+  return b;
+}
+
+cudaError_t small_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(k_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_small, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+// Clusters of `cs` CTAs that can run at once with `smem` bytes a CTA.
+int small_active_clusters(int cs, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_small, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream) {
+  if (p.cs != 8 && p.cs != 16) return cudaErrorInvalidValue;
+  const int b_max = small_tokens_max(p.hidden, p.tp, p.cs);
+  if (b_max < 1 || clusters < 1 || (p.m + clusters - 1) / clusters > b_max || !p.hc_fn) return cudaErrorInvalidValue;
+  if (p.cols_max != small_cols_max(p.hidden, p.cs)) return cudaErrorInvalidValue;
+  const int b = (p.m + clusters - 1) / clusters;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * p.cs);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = small_smem_bytes(p.hidden, p.tp, p.cs, b);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_small, p);
+}
+
+}  // namespace mhc

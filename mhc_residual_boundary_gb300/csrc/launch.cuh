@@ -75,6 +75,39 @@ struct FinishParams {
   unsigned int *err;          // device error word (bit 1: a wait gave up) or null
 };
 
+// The boundary of a few tokens in one kernel (k_small.cu): clusters of `cs`
+// CTAs, each cluster up to SMALL_B_MAX tokens, each CTA a column range.
+constexpr int SMALL_B_MAX = 8;
+constexpr int SMALL_ITEMS_MAX = 512;   // (token, 16-byte fragment) items of a CTA
+// Largest call the one-kernel path takes (larger calls run the stage and
+// finish kernels).
+constexpr int SMALL_M_MAX = 128;
+struct SmallParams {
+  int m, hidden, tp;
+  int cs;                     // CTAs a cluster (8 or 16)
+  int cols_max;               // small_cols_max(hidden, cs)
+  const uint16_t *partials;   // [tp][m][H]
+  const uint16_t *residual;   // [m][4][H]
+  const float *post;          // [m][4]
+  const float *comb;          // [m][4][4]
+  const float *hc_fn;         // [4H][24] f32
+  const float *scale;         // [3]
+  const float *base;          // [24]
+  const uint16_t *gamma;      // [H]
+  int early_weight;           // the weight is a layer weight: load it before the wait
+  float rms_eps, hc_eps, norm_eps, post_mult;
+  int repeat;
+  uint16_t *residual_out;     // [m][4][H]
+  uint16_t *reduced_out;      // [m][H] or null
+  uint16_t *layer_input;      // [m][H]
+  float *mixes;               // [m][24] for a separate post / Sinkhorn kernel, or null
+  float *mixes_out, *pre_out; // optional
+  float *post_out, *comb_out; // null when a separate kernel computes them
+  uint8_t *mx_values;         // [m][H] or null
+  uint8_t *mx_scales;         // mxfp8_scale_bytes(m, H) or null
+  unsigned int *err;          // bit 1: a copy wait gave up
+};
+
 // Two-shot reduction (single-GPU emulation of the owner reduce): the tp
 // partials [tp][m][H] summed per token into sums [m][H].
 struct OwnerParams {
@@ -121,6 +154,16 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
 cudaError_t finish_set_attributes();
 cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl);
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
+// The boundary of a few tokens in one kernel: columns a CTA, shared memory,
+// tokens a cluster (0: the shape does not fit), attributes, clusters that
+// run at once, launch on `clusters` clusters.
+int small_cols_max(int hidden, int cs);
+size_t small_smem_bytes(int hidden, int tp, int cs, int tokens);
+int small_tokens_max(int hidden, int tp, int cs);
+cudaError_t small_set_attributes();
+cudaError_t small_stall_copies(int on);   // test hook, see include/mhc_boundary_test.h
+int small_active_clusters(int cs, size_t smem);
+cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream);
 // MoE fold over at most `ctas` CTAs of 128 threads.
 cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream);
 cudaError_t launch_owner_reduce(const OwnerParams &p, int ctas, cudaStream_t stream);

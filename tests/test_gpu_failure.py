@@ -1,5 +1,5 @@
-"""Failure detection on the GPU without a fault: a stage kernel whose input
-copies never come gives up its bounded waits, the host reads
+"""Failure detection on the GPU without a fault: a boundary kernel whose
+input copies never come gives up its bounded waits, the host reads
 MHC_ERR_TIMEOUT from the error word, and the same handle and context then
 compute correct results again."""
 import numpy as np
@@ -13,11 +13,13 @@ from mhc_residual_boundary_gb300 import capi, synth
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_copies_report_a_timeout_and_the_handle_recovers():
+# 40 tokens take the one-kernel path, 200 the stage and finish kernels
+@pytest.mark.parametrize("m", [40, 200])
+def test_stalled_copies_report_a_timeout_and_the_handle_recovers(m):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     from mhc_residual_boundary_gb300 import Boundary
-    hidden, tp, m = 1024, 4, 40
+    hidden, tp = 1024, 4
     inp = synth.make_inputs(hidden, tp, m, seed=77)
     ref = oracle_outputs(oracle.Problem(hidden, tp, m), inp)
     b = Boundary(hidden=hidden, tp=tp, max_num_tokens=m)

@@ -35,7 +35,9 @@ def test_owner_reduce_same_bits(Boundary, hidden, tp, m, mxfp8):
         try:
             outs[owner] = run_gpu(b, inp, mxfp8=mxfp8)
             b.check_errors()
-            assert b.launches_per_call() == 2 + int(owner)
+            # the owner reduce adds one kernel before the boundary's one (a few
+            # tokens) or two (stage and finish)
+            assert b.launches_per_call() - int(owner) in (1, 2)
         finally:
             b.close()
     # the stage-1 sums and the post-mixed streams are the same bits; with at
