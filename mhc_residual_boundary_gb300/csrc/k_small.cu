@@ -19,21 +19,24 @@
 //      FP32 weight, split over threads by (4 outputs, row phase) with every
 //      token of the cluster in each thread (the weight is read once), summed
 //      back in a fixed shuffle tree;
-//   4. cluster barrier; every CTA sums the CS partials of each token in rank
-//      order from the other CTAs' shared memory, then rstd, mixes and pre
+//   4. every CTA sends its partial sums of each token into every CTA's
+//      inbox (remote stores that count their bytes on the receiver's
+//      mbarrier), then sums its own inbox in rank order: rstd, mixes and pre
 //      ([GLM] "rstd", "pre_mix") -- the same values in every CTA;
 //   5. collapse c = bf16((n0 p0 + n1 p1) + (n2 p2 + n3 p3)) of its columns
-//      and their sum of c^2; cluster barrier; inv_rms from the CS sums in rank
-//      order; out = bf16((c * inv_rms) * gamma) and the optional MXFP8 copy
-//      ([GLM] "collapse", "inv_rms"; [DSV] quantize branch);
+//      and their sum of c^2, exchanged the same way; inv_rms from the CS sums
+//      in rank order; out = bf16((c * inv_rms) * gamma) and the optional MXFP8
+//      copy ([GLM] "collapse", "inv_rms"; [DSV] quantize branch);
 //   6. token t's post and Sinkhorn mix ([GLM] _MixesDeviceKernel) in four
 //      lanes of CTA rank t % CS's last warp (the same operations as the
 //      finish kernel's, so the same bits), from right after step 4, while
 //      the other warps collapse and normalise.
-// A last cluster barrier keeps every CTA's shared memory alive until the
-// others have read it.  The copy waits are bounded; a CTA whose copies do not
-// arrive skips its work (its outputs are invalid), still takes part in every
-// cluster barrier, and sets bit 1 of the error word.
+// One cluster barrier, after every CTA has armed its inboxes, orders the
+// first remote store after the arming; a CTA leaves only once its inboxes
+// are complete, so no store reaches a CTA that has left.  Every wait is
+// bounded; a CTA whose copies do not arrive skips its work (its outputs are
+// invalid), still sends (zeros) to every inbox, and sets bit 1 of the error
+// word.
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
@@ -57,12 +60,17 @@ constexpr int GEMV_ROWS_WARP = 5;              // weight rows a warp takes at on
 constexpr int GEMV_ROWS_PASS = GEMV_ROWS_WARP * NWARP;   // 80
 constexpr uint32_t WAIT_LIMIT = 1u << 22;      // polls before a copy wait gives up
 constexpr int SMEM_MAX = 227 * 1024;
+constexpr int IN1_STRIDE = 28;                 // floats of a token's partials in an inbox (7 x 16 bytes)
 
 // Shared memory: control block, then the weight rows, then one slot per token.
 struct Ctl {
   static constexpr int wbar = 0;               // uint64: weight rows arrived
   static constexpr int dbar = 8;               // uint64: token data arrived
-  static constexpr int red = 16;               // f32 [SMALL_B_MAX][25]: GEMV partials + sum of squares
+  static constexpr int ibar1 = 16;             // uint64: every CTA's GEMV partials arrived
+  static constexpr int ibar2 = 24;             // uint64: every CTA's sums of c^2 arrived
+  static constexpr int inbox1 = 32;            // f32 [16 ranks][SMALL_B_MAX][28]: partials + sum of squares (padded)
+  static constexpr int inbox2 = inbox1 + 16 * SMALL_B_MAX * IN1_STRIDE * 4;   // f32 [16 ranks][8]: sums of c^2
+  static constexpr int red = inbox2 + 16 * 8 * 4;   // f32 [SMALL_B_MAX][25]: GEMV partials + sum of squares
   static constexpr int red2 = red + SMALL_B_MAX * VALUES * 4;   // f32 [SMALL_B_MAX]: sum of c^2
   static constexpr int pre = red2 + SMALL_B_MAX * 4;             // f32 [SMALL_B_MAX][4]
   static constexpr int ir = pre + SMALL_B_MAX * 16;              // f32 [SMALL_B_MAX]
@@ -94,18 +102,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 }
 // Every thread of every CTA of the cluster: arrive (release), then wait (acquire).
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync() {
   cluster_arrive();
   cluster_wait();
-}
-// A float of cluster CTA `rank`'s shared memory at this CTA's address `p`.
-__device__ __forceinline__ float ld_cluster(const void *p, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_addr(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
 }
 
 // The 15 warps other than the post / Sinkhorn warp.
@@ -116,6 +119,20 @@ __device__ __forceinline__ float tree_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// This CTA's shared address `p` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t remote_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(tc::smem_addr(p)), "r"(rank));
+  return r;
+}
+// 16 bytes into cluster shared memory, counted in bytes on the receiver's
+// mbarrier when they land.
+__device__ __forceinline__ void st_async16(uint32_t remote, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+               ::"r"(remote), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
 }
 
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
@@ -197,13 +214,26 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   unsigned char *slots = w_s + weight_bytes(p.cols_max);
   const int sbytes = slot_bytes(tp, p.cols_max);
 
+  uint64_t *ibar1 = reinterpret_cast<uint64_t *>(smem + Ctl::ibar1);
+  uint64_t *ibar2 = reinterpret_cast<uint64_t *>(smem + Ctl::ibar2);
+  float *inbox1 = reinterpret_cast<float *>(smem + Ctl::inbox1);
+  float *inbox2 = reinterpret_cast<float *>(smem + Ctl::inbox2);
+  const int in2_vecs = (b + 3) / 4;   // 16-byte pieces of a CTA's sums of c^2
   if (tid == 0) {
     tc::mbar_init(wbar, 1);
     tc::mbar_init(dbar, 1);
+    tc::mbar_init(ibar1, 1);
+    tc::mbar_init(ibar2, 1);
     *bad = 0;
     tc::mbar_init_fence();
+    // the inboxes expect every CTA's pieces
+    if (b > 0) {
+      tc::mbar_arrive_expect_tx(ibar1, uint32_t(cs * b * IN1_STRIDE * 4));
+      tc::mbar_arrive_expect_tx(ibar2, uint32_t(cs * in2_vecs * 16));
+    }
   }
-  __syncthreads();
+  // every CTA's inboxes are armed before any CTA sends
+  cluster_sync();
   pdl_launch_dependents();
 
   // the weight rows of this CTA's columns (a layer weight: before the wait)
@@ -343,17 +373,29 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     for (int w = 0; w < NWARP; ++w) v = __fadd_rn(v, gred[((w * SMALL_B_MAX) + t) * MIX + i]);
     red[t * VALUES + i] = v;
   }
-  // ---- 4. the cluster's sums, rank order; rstd, mixes, pre
-  cluster_sync();
+  __syncthreads();
+  // ---- 4. this CTA's partials of every token into every CTA's inbox (slot
+  // `rank`): thread (peer, token, 16-byte piece)
+  {
+    constexpr int PIECES = IN1_STRIDE / 4;
+    for (int e = tid; e < cs * b * PIECES; e += NT) {
+      const int peer = e / (b * PIECES), rest = e % (b * PIECES), t = rest / PIECES, k = rest % PIECES;
+      const float *src = red + t * VALUES + k * 4;
+      float4 v;
+      v.x = k * 4 + 0 < VALUES ? src[0] : 0.f;
+      v.y = k * 4 + 1 < VALUES ? src[1] : 0.f;
+      v.z = k * 4 + 2 < VALUES ? src[2] : 0.f;
+      v.w = k * 4 + 3 < VALUES ? src[3] : 0.f;
+      const float *dst = inbox1 + ((int(rank) * SMALL_B_MAX) + t) * IN1_STRIDE + k * 4;
+      st_async16(remote_addr(dst, uint32_t(peer)), v, remote_addr(ibar1, uint32_t(peer)));
+    }
+  }
+  // every CTA's partials, summed in rank order; rstd, mixes, pre
+  if (b > 0 && !tc::mbar_wait_bounded(ibar1, 0u, WAIT_LIMIT)) *bad = 1;
   if (warp < b) {
-    // the cs partials first (independent loads), then their sum in rank order
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) x[r] = lane < VALUES && r < cs ? ld_cluster(red + warp * VALUES + lane, uint32_t(r)) : 0.f;
     float v = 0.f;
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < cs) v = __fadd_rn(v, x[r]);
+    if (lane < VALUES)
+      for (int r = 0; r < cs; ++r) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + warp) * IN1_STRIDE + lane]);
     const int t = t0 + warp;
     const float ss = __shfl_sync(0xffffffffu, v, MIX);
     const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
@@ -374,11 +416,11 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
 
   // ---- 5. collapse of this CTA's columns (kept in registers for step 7);
   // meanwhile the last warp runs post and the Sinkhorn mix of this CTA's
-  // tokens (it has no items and arrives at the next cluster barrier early)
+  // tokens (it has no items and sends nothing more)
   constexpr int IPT = (SMALL_ITEMS_MAX + ITEM_THREADS - 1) / ITEM_THREADS;   // items a thread
   uint32_t cw[IPT][4];
   if (warp == SINK_WARP) {
-    cluster_arrive();
+    cluster_arrive_relaxed();
     if (p.post_out) {
       // tokens t of this cluster with t % cs == rank, one a quad of lanes
       const int first = (int(rank) - t0 % cs + cs) % cs;   // first local index with (t0 + i) % cs == rank
@@ -389,7 +431,6 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
         post_and_sinkhorn4(ma, t0 + (live ? i : 0), mix_s + (live ? i : 0) * MIX, live);
       }
     }
-    cluster_wait();
   } else {
 #pragma unroll
     for (int n = 0; n < IPT; ++n) {
@@ -426,22 +467,32 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
       s = tree_sum(s);
       if (lane == 0) red2[warp] = s;
     }
-    // the norm-weight fragments, requested before the barrier
+    item_sync();
+    // ---- 6. this CTA's sums of c^2 into every CTA's inbox (slot `rank`)
+    if (tid < cs * in2_vecs) {
+      const int peer = tid / in2_vecs, k = tid % in2_vecs;
+      float4 v;
+      v.x = k * 4 + 0 < b ? red2[k * 4 + 0] : 0.f;
+      v.y = k * 4 + 1 < b ? red2[k * 4 + 1] : 0.f;
+      v.z = k * 4 + 2 < b ? red2[k * 4 + 2] : 0.f;
+      v.w = k * 4 + 3 < b ? red2[k * 4 + 3] : 0.f;
+      st_async16(remote_addr(inbox2 + int(rank) * 8 + k * 4, uint32_t(peer)), v, remote_addr(ibar2, uint32_t(peer)));
+    }
+    // this CTA sends nothing more
+    cluster_arrive_relaxed();
+    // the norm-weight fragments, requested before the wait
     uint4 gw[IPT];
 #pragma unroll
     for (int n = 0; n < IPT; ++n) {
       const int item = tid + n * ITEM_THREADS;
       gw[n] = ok && item < n_items ? ld_ro(p.gamma + c0 + (item % F) * VEC) : make_uint4(0u, 0u, 0u, 0u);
     }
-    // ---- 6. cluster barrier
-    cluster_arrive();
-    cluster_wait();
     // ---- 7. inv_rms of each token (the CS sums in rank order), normalisation
-    if (warp < b) {
-      const float x = lane < cs ? ld_cluster(red2 + warp, uint32_t(lane)) : 0.f;
+    if (b > 0 && !tc::mbar_wait_bounded(ibar2, 0u, WAIT_LIMIT)) *bad = 1;
+    if (warp < b && lane == 0) {
       float s = 0.f;
-      for (int r = 0; r < cs; ++r) s = __fadd_rn(s, __shfl_sync(0xffffffffu, x, r));
-      if (lane == 0) ir_s[warp] = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(s, float(H)), p.norm_eps)));
+      for (int r = 0; r < cs; ++r) s = __fadd_rn(s, inbox2[r * 8 + warp]);
+      ir_s[warp] = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(s, float(H)), p.norm_eps)));
     }
     item_sync();
     const int scols = H / 32;
@@ -489,9 +540,10 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
       for (int c4 = tid; c4 < scols / 4; c4 += NT)
         *reinterpret_cast<uint32_t *>(p.mx_scales + swizzle_128x4(row, c4 * 4, scols)) = 0u;
   }
-  if (tid == 0 && !ok && p.err) atomicOr(p.err, 2u);
-  // no CTA leaves while another may still read its shared memory
-  cluster_sync();
+  // no CTA leaves before every CTA has issued its remote stores (its own
+  // inboxes are complete, so nothing more arrives here)
+  cluster_wait();
+  if (tid == 0 && *bad != 0 && p.err) atomicOr(p.err, 2u);
 }
 
 }  // namespace

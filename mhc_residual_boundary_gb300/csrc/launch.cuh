@@ -80,8 +80,10 @@ struct FinishParams {
 constexpr int SMALL_B_MAX = 8;
 constexpr int SMALL_ITEMS_MAX = 512;   // (token, 16-byte fragment) items of a CTA
 // Largest call the one-kernel path takes (larger calls run the stage and
-// finish kernels).
-constexpr int SMALL_M_MAX = 128;
+// finish kernels).  Beyond eight tokens its clusters hold most of the SMs, so
+// the next call's CTAs cannot start their prologue beside it, and the stage
+// and finish kernels are as fast (measured at H = 5120-7168, tp = 4 and 8).
+constexpr int SMALL_M_MAX = 8;
 struct SmallParams {
   int m, hidden, tp;
   int cs;                     // CTAs a cluster (8 or 16)

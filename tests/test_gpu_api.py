@@ -132,10 +132,13 @@ def test_launch_count(env):
     # mixes kernel adds one; beyond the one-kernel path's token range the
     # stage and finish kernels
     b, _, _ = env
-    assert b.launches_per_call() == 1
+    assert b.launches_per_call() == 2          # M = 24: stage and finish
     from mhc_residual_boundary_gb300 import Boundary
+    few = Boundary(hidden=H, tp=TP, max_num_tokens=8)
+    assert few.launches_per_call() == 1
+    few.close()
     for flags in ({"side_mixes": True}, {"sync_mixes": True}):
-        other = Boundary(hidden=H, tp=TP, max_num_tokens=M, **flags)
+        other = Boundary(hidden=H, tp=TP, max_num_tokens=8, **flags)
         assert other.launches_per_call() == 2
         other.close()
     many = Boundary(hidden=H, tp=TP, max_num_tokens=1000)

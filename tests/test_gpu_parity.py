@@ -104,6 +104,14 @@ def test_few_tokens(Boundary, hidden, tp, m, bf16):
     check(Boundary, hidden, tp, m, bf16_weight=bf16, mxfp8=hidden % 128 == 0, seed=hidden + 3 * m)
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("m", range(1, 10))
+def test_one_to_nine_tokens(Boundary, m, bf16):
+    # the GLM shape around the one-kernel path's range (FP32 weight, up to
+    # eight tokens) and the stage and finish kernels beside it
+    check(Boundary, 6144, 4, m, bf16_weight=bf16, mxfp8=True, seed=31 * m + bf16)
+
+
 @pytest.mark.parametrize("hidden,tp,m,bf16", [(2048, 6, 1024, False), (2048, 3, 1024, False),
                                               (6144, 8, 512, True), (2048, 8, 1024, True),
                                               (5120, 8, 2000, False)])
@@ -150,12 +158,13 @@ def test_static_weight(Boundary, hidden, tp, m, bf16, moe):
           mxfp8=hidden % 128 == 0, flags={"static_weight": True}, seed=hidden + m)
 
 
-def test_static_weight_chained_calls_match(Boundary):
+@pytest.mark.parametrize("m", [5, 48])
+def test_static_weight_chained_calls_match(Boundary, m):
     # each call reads the previous call's residual_out, post_out and comb_out
-    # on the same stream, while its stage kernel may start during the
-    # previous finish kernel: the chain gives the bits of the chain without
-    # the early staging
-    hidden, tp, m, calls = 2048, 4, 48, 12
+    # on the same stream, while its kernel may start during the previous
+    # call's last kernel: the chain gives the bits of the chain without the
+    # early staging (5 tokens: the one-kernel path; 48: stage and finish)
+    hidden, tp, calls = 2048, 4, 12
     inp = to_device(synth.make_inputs(hidden, tp, m, seed=21))
     results = {}
     for static in (False, True):
@@ -181,13 +190,15 @@ MIXES_PLACEMENTS = {"fused": {}, "side": {"side_mixes": True}, "sync": {"sync_mi
                     "static": {"static_weight": True}}
 
 
-def test_mixes_placements_give_same_bits(Boundary):
-    # post / Sinkhorn inside the finish kernel, in the side-stream kernel and
-    # in the same kernel on the caller's stream take the same operations
-    inp = synth.make_inputs(1024, 4, 50, seed=3)
+@pytest.mark.parametrize("m", [6, 50])
+def test_mixes_placements_give_same_bits(Boundary, m):
+    # post / Sinkhorn inside the boundary kernel (the one-kernel path at 6
+    # tokens, the finish kernel at 50), in the side-stream kernel and in the
+    # same kernel on the caller's stream take the same operations
+    inp = synth.make_inputs(1024, 4, m, seed=3)
     outs = {}
     for name, flags in MIXES_PLACEMENTS.items():
-        b = Boundary(hidden=1024, tp=4, max_num_tokens=50, **flags)
+        b = Boundary(hidden=1024, tp=4, max_num_tokens=m, **flags)
         outs[name] = run_gpu(b, inp)
         b.close()
     for name in outs["fused"]:
