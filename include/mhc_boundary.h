@@ -281,9 +281,16 @@ mhc_status_t mhc_boundary_join(mhc_boundary_t *b, mhc_stream_t stream);
 
 /* mhc_boundary_run with HOST pointers in `args` (every tensor in host
  * memory; pinned memory makes the copies asynchronous).  Needs
- * MHC_FLAG_HOST_STAGING.  Copies the inputs to library staging buffers on
- * `stream`, runs, joins, copies the outputs back and synchronises `stream`
- * before returning (so it cannot be captured). */
+ * MHC_FLAG_HOST_STAGING.  The call is split into token chunks (one chunk
+ * below 512 tokens, else up to 8 chunks of at least 256 tokens, each a
+ * multiple of 128): each chunk's inputs are copied to the library staging
+ * buffers on the handle's host-to-device stream, its kernels run on `stream`
+ * once they have arrived, and its outputs are copied back on the handle's
+ * device-to-host stream, so copies in both directions overlap the kernels.
+ * Each chunk is one boundary call over its tokens (the same bits as one
+ * call over all of them).  The copy streams start after the work already on
+ * `stream`, and the call synchronises `stream`, which is ordered after the
+ * last copy, before returning (so it cannot be captured). */
 mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *args,
                                    mhc_stream_t stream);
 

@@ -15,6 +15,7 @@
 //
 // Pages: [GLM] vllm.models.glm5next.nvidia.specialized_decode.all_reduce_mhc,
 //        [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -28,6 +29,12 @@
 #include "mhc_boundary_test.h"
 
 using namespace mhc;
+
+// mhc_boundary_run_host splits a call into up to HOST_CHUNKS_MAX token
+// chunks of at least HOST_CHUNK_MIN tokens (multiples of 128, so that each
+// chunk's MXFP8 scales are one contiguous run of the swizzled layout).
+constexpr int HOST_CHUNKS_MAX = 8;
+constexpr int HOST_CHUNK_MIN = 256;
 
 struct mhc_boundary {
   mhc_boundary_config_t cfg;
@@ -51,6 +58,11 @@ struct mhc_boundary {
   int small_clusters = 0;
   unsigned char *staging = nullptr;
   size_t staging_bytes = 0;
+  // mhc_boundary_run_host's pipeline: copy streams in each direction and the
+  // events that hand each token chunk from copy to compute to copy
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t host_start = nullptr, host_end = nullptr;
+  cudaEvent_t in_done[HOST_CHUNKS_MAX] = {}, run_done[HOST_CHUNKS_MAX] = {};
   // profiling: 6 events per recorded call (stage, finish, mixes: start/end)
   std::vector<cudaEvent_t> prof_events;
   int prof_capacity = 0;
@@ -528,6 +540,14 @@ void release(mhc_boundary *b) {
   if (b->side) cudaStreamSynchronize(b->side);
   destroy_profile_events(b);
   if (b->staging) cudaFree(b->staging);
+  for (int k = 0; k < HOST_CHUNKS_MAX; ++k) {
+    if (b->in_done[k]) cudaEventDestroy(b->in_done[k]);
+    if (b->run_done[k]) cudaEventDestroy(b->run_done[k]);
+  }
+  if (b->host_start) cudaEventDestroy(b->host_start);
+  if (b->host_end) cudaEventDestroy(b->host_end);
+  if (b->h2d) cudaStreamDestroy(b->h2d);
+  if (b->d2h) cudaStreamDestroy(b->d2h);
   if (b->mixes) cudaFree(b->mixes);
   if (b->part) cudaFree(b->part);
   if (b->fold) cudaFree(b->fold);
@@ -606,6 +626,14 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   if (e == cudaSuccess && (c.flags & MHC_FLAG_HOST_STAGING)) {
     b->staging_bytes = staging_layout(c).total;
     e = cudaMalloc(&b->staging, b->staging_bytes);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&b->d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->host_start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->host_end, cudaEventDisableTiming);
+    for (int k = 0; k < HOST_CHUNKS_MAX && e == cudaSuccess; ++k) {
+      e = cudaEventCreateWithFlags(&b->in_done[k], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b->run_done[k], cudaEventDisableTiming);
+    }
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -706,36 +734,103 @@ mhc_status_t mhc_boundary_run_host(mhc_boundary_t *b, const mhc_run_args_t *host
   }
   DeviceGuard guard(b->device);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // Token chunks: chunk k's inputs go up on the h2d stream, its kernels run on
+  // `stream` once they are there, and its outputs come back on the d2h
+  // stream once the kernels are done, so the copies of one chunk overlap the
+  // kernels and the opposite-direction copies of its neighbours.  Chunk k
+  // uses its own part of every staging buffer ([tp][mc][H] partials at tp *
+  // t0 * H, the other tensors at their token offset), so no chunk waits for
+  // another's buffers.
+  const int n_chunks = std::max(1, std::min(HOST_CHUNKS_MAX, m / HOST_CHUNK_MIN));
+  const int per_chunk = (m + n_chunks - 1) / n_chunks;
+  const int chunk = n_chunks == 1 ? m : (per_chunk + 127) / 128 * 128;
+  // chunk k: tokens [t0s[k], t0s[k] + mcs[k]); a tail under 128 tokens joins
+  // the chunk before it, so that every chunk takes the same kernels as the
+  // whole call would
+  int t0s[HOST_CHUNKS_MAX], mcs[HOST_CHUNKS_MAX], nk = 0;
+  for (int t0 = 0; t0 < m && nk < HOST_CHUNKS_MAX; t0 += mcs[nk++]) {
+    t0s[nk] = t0;
+    mcs[nk] = std::min(chunk, m - t0);
+    if (m - (t0 + mcs[nk]) < 128 || nk == HOST_CHUNKS_MAX - 1) mcs[nk] = m - t0;
+  }
+  const int tp = c.tp;
+  auto ptr = [](const void *p, size_t off) -> const unsigned char * {
+    return p ? static_cast<const unsigned char *>(p) + off : nullptr;
+  };
+  auto mptr = [](void *p, size_t off) -> unsigned char * {
+    return p ? static_cast<unsigned char *>(p) + off : nullptr;
+  };
+  cudaError_t e = cudaEventRecord(b->host_start, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(b->h2d, b->host_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(b->d2h, b->host_start, 0);
+  // the call's weights once, before the first chunk's inputs
   struct Copy { void *dst; const void *src; size_t bytes; };
-  const Copy in[] = {
-      {base + L.partials, host->partials, size_t(c.tp) * M * H * 2},
-      {base + L.residual, host->residual, M * HC * H * 2},
-      {base + L.post, host->post, M * HC * 4},
-      {base + L.comb, host->comb, M * HC * HC * 4},
+  const Copy weights[] = {
       {base + L.hc_fn, host->hc_fn ? static_cast<const void *>(host->hc_fn) : host->hc_fn_bf16,
        size_t(HC) * H * MIX * (host->hc_fn ? 4 : 2)},
       {base + L.scale, host->scale, 3 * 4},
       {base + L.base, host->base, MIX * 4},
       {base + L.gamma, host->norm_weight, H * 2}};
-  cudaError_t e = cudaSuccess;
-  for (const Copy &x : in)
-    if (e == cudaSuccess) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyHostToDevice, stream);
+  for (const Copy &x : weights)
+    if (e == cudaSuccess && x.src) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyHostToDevice, b->h2d);
+  for (int k = 0; k < nk && e == cudaSuccess; ++k) {
+    const size_t T0 = size_t(t0s[k]), MC = size_t(mcs[k]);
+    // partials: tp row runs of mc x H, one 2-D copy (host rows m x H apart)
+    if (host->partials)
+      e = cudaMemcpy2DAsync(base + L.partials + size_t(tp) * T0 * H * 2, MC * H * 2,
+                            ptr(host->partials, T0 * H * 2), M * H * 2, MC * H * 2, size_t(tp),
+                            cudaMemcpyHostToDevice, b->h2d);
+    const Copy in[] = {{base + L.residual + T0 * HC * H * 2, ptr(host->residual, T0 * HC * H * 2), MC * HC * H * 2},
+                       {base + L.post + T0 * HC * 4, ptr(host->post, T0 * HC * 4), MC * HC * 4},
+                       {base + L.comb + T0 * HC * HC * 4, ptr(host->comb, T0 * HC * HC * 4), MC * HC * HC * 4}};
+    for (const Copy &x : in)
+      if (e == cudaSuccess && x.src) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyHostToDevice, b->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(b->in_done[k], b->h2d);
+  }
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "host to device copy: %s", cudaGetErrorString(e));
-  s = launch_call(b, &d, nullptr, stream);
-  if (s != MHC_OK) return s;
-  if (b->side_pending) e = cudaStreamWaitEvent(stream, b->side_done, 0);
-  const Copy out[] = {
-      {host->residual_out, d.residual_out, M * HC * H * 2},
-      {host->layer_input, d.layer_input, M * H * 2},
-      {host->post_out, d.post_out, M * HC * 4},
-      {host->comb_out, d.comb_out, M * HC * HC * 4},
-      {host->pre_out, d.pre_out, M * HC * 4},
-      {host->mixes_out, d.mixes_out, M * MIX * 4},
-      {host->reduced_out, d.reduced_out, M * H * 2},
-      {host->mxfp8_values, d.mxfp8_values, M * H},
-      {host->mxfp8_scales, d.mxfp8_scales, scale_bytes(m, c.hidden)}};
-  for (const Copy &x : out)
-    if (e == cudaSuccess && x.dst) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyDeviceToHost, stream);
+  for (int k = 0; k < nk; ++k) {
+    const size_t T0 = size_t(t0s[k]);
+    mhc_run_args_t dk = d;
+    dk.m = mcs[k];
+    dk.partials = mptr(const_cast<void *>(d.partials), size_t(tp) * T0 * H * 2);
+    dk.residual = mptr(const_cast<void *>(d.residual), T0 * HC * H * 2);
+    dk.post = reinterpret_cast<float *>(mptr(const_cast<float *>(d.post), T0 * HC * 4));
+    dk.comb = reinterpret_cast<float *>(mptr(const_cast<float *>(d.comb), T0 * HC * HC * 4));
+    dk.residual_out = mptr(d.residual_out, T0 * HC * H * 2);
+    dk.layer_input = mptr(d.layer_input, T0 * H * 2);
+    dk.post_out = reinterpret_cast<float *>(mptr(d.post_out, T0 * HC * 4));
+    dk.comb_out = reinterpret_cast<float *>(mptr(d.comb_out, T0 * HC * HC * 4));
+    dk.pre_out = reinterpret_cast<float *>(mptr(d.pre_out, T0 * HC * 4));
+    dk.mixes_out = reinterpret_cast<float *>(mptr(d.mixes_out, T0 * MIX * 4));
+    dk.reduced_out = mptr(d.reduced_out, T0 * H * 2);
+    dk.mxfp8_values = reinterpret_cast<uint8_t *>(mptr(d.mxfp8_values, T0 * H));
+    dk.mxfp8_scales = reinterpret_cast<uint8_t *>(mptr(d.mxfp8_scales, T0 * (H / 32)));
+    e = cudaStreamWaitEvent(stream, b->in_done[k], 0);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "copy wait: %s", cudaGetErrorString(e));
+    s = launch_call(b, &dk, nullptr, stream);
+    if (s != MHC_OK) return s;
+    if (b->side_pending) e = cudaStreamWaitEvent(stream, b->side_done, 0);
+    if (e == cudaSuccess) e = cudaEventRecord(b->run_done[k], stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "chunk event: %s", cudaGetErrorString(e));
+  }
+  for (int k = 0; k < nk && e == cudaSuccess; ++k) {
+    const size_t T0 = size_t(t0s[k]), MC = size_t(mcs[k]);
+    e = cudaStreamWaitEvent(b->d2h, b->run_done[k], 0);
+    const Copy out[] = {
+        {mptr(host->residual_out, T0 * HC * H * 2), ptr(d.residual_out, T0 * HC * H * 2), MC * HC * H * 2},
+        {mptr(host->layer_input, T0 * H * 2), ptr(d.layer_input, T0 * H * 2), MC * H * 2},
+        {mptr(host->post_out, T0 * HC * 4), ptr(d.post_out, T0 * HC * 4), MC * HC * 4},
+        {mptr(host->comb_out, T0 * HC * HC * 4), ptr(d.comb_out, T0 * HC * HC * 4), MC * HC * HC * 4},
+        {mptr(host->pre_out, T0 * HC * 4), ptr(d.pre_out, T0 * HC * 4), MC * HC * 4},
+        {mptr(host->mixes_out, T0 * MIX * 4), ptr(d.mixes_out, T0 * MIX * 4), MC * MIX * 4},
+        {mptr(host->reduced_out, T0 * H * 2), ptr(d.reduced_out, T0 * H * 2), MC * H * 2},
+        {mptr(host->mxfp8_values, T0 * H), ptr(d.mxfp8_values, T0 * H), MC * H},
+        {mptr(host->mxfp8_scales, T0 * (H / 32)), ptr(d.mxfp8_scales, T0 * (H / 32)), scale_bytes(mcs[k], c.hidden)}};
+    for (const Copy &x : out)
+      if (e == cudaSuccess && x.dst) e = cudaMemcpyAsync(x.dst, x.src, x.bytes, cudaMemcpyDeviceToHost, b->d2h);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(b->host_end, b->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, b->host_end, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "device to host copy: %s", cudaGetErrorString(e));
   return MHC_OK;

@@ -234,10 +234,14 @@ def test_back_to_back_calls_chain_mixes(Boundary, placement):
     compare(got2, ref2, inp2)
 
 
-def test_run_host_matches_run(Boundary):
-    hidden, tp, m = 1024, 4, 33
+@pytest.mark.parametrize("m,flags", [(33, {}), (1000, {}), (2048, {"side_mixes": True}), (700, {"static_weight": True})])
+def test_run_host_matches_run(Boundary, m, flags):
+    # one chunk (33 tokens) and the pipelined token chunks: 1000 tokens as
+    # 384 + 384 + 232, 2048 as eight 256-token chunks with the side-stream
+    # mixes kernel, 700 as 384 + 316; the same bits as the device-buffer call
+    hidden, tp = 1024, 4
     inp = synth.make_inputs(hidden, tp, m, seed=8)
-    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=64, host_staging=True, mxfp8=True)
+    b = Boundary(hidden=hidden, tp=tp, max_num_tokens=max(m, 64), host_staging=True, mxfp8=True, **flags)
     dev_out = run_gpu(b, inp, mxfp8=True)
     host_in = {k: v.pin_memory() for k, v in to_device(inp, device="cpu").items()}
     host_out = b.empty_outputs(m, extras=True, mxfp8=True, device="cpu", pin_memory=True)
