@@ -209,7 +209,16 @@ __global__ void __launch_bounds__(NT, NF <= 5 ? 4 : NF <= 7 ? 3 : NF <= 9 ? 2 : 
       const int b = k % BATCH;
       if (p.post_out && !p.pre_in && (b == BATCH - 1 || k == n_tok - 1)) {
         const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
-        if (lane <= b) post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
+        if (b < 8) {
+          // a batch of at most 8 tokens (a CTA's last, or all it has at
+          // small M, where the chain sits on the CTA's critical path): four
+          // lanes a token, a shorter chain with the same bits
+          const int i = lane >> 2;
+          post_and_sinkhorn4(ma, int(blockIdx.x) + (k - b + (i <= b ? i : 0)) * int(gridDim.x),
+                             mix_s[i <= b ? i : 0], i <= b);
+        } else if (lane <= b) {
+          post_and_sinkhorn(ma, int(blockIdx.x) + (k - b + lane) * int(gridDim.x), mix_s[lane]);
+        }
         __syncwarp();
       }
       // steps 1-2 of the next token, beside this token's collapse (its
