@@ -92,9 +92,16 @@ __device__ __forceinline__ float sigmoid(float z) {
   return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
 }
 
-// The Sinkhorn normalisation reciprocal: CUDA's fast approximate division
-// (within 2 ulp of 1/x for the positive sums it takes).
-__device__ __forceinline__ float rcp_fast(float x) { return __fdividef(1.0f, x); }
+// The Sinkhorn normalisation reciprocal: the hardware's approximate
+// reciprocal instruction (rcp.approx, within 1 ulp of 1/x; the sums it takes
+// are at least eps = 1e-6 and at most a few units, far from subnormal, so
+// the flush-to-zero form is exact in its range).  One instruction on the
+// chain of 40 dependent normalisations a token.
+__device__ __forceinline__ float rcp_fast(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 // A BF16 pair as FP32 (exact).
 __device__ __forceinline__ float2 bf16_pair(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
@@ -182,23 +189,26 @@ static __device__ __noinline__ void post_and_sinkhorn(const MixArgs p, int t, co
 #pragma unroll
     for (int k = 0; k < HC; ++k) x[k] = __fadd_rn(__fmul_rn(x[k], inv), eps);
   }
-#pragma unroll 1
-  for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) {
-#pragma unroll
-      for (int r = 0; r < HC; ++r) {
-        float *x = c + HC * r;
-        const float inv = rcp_fast(__fadd_rn(sum4_paired(x[0], x[1], x[2], x[3]), eps));
-#pragma unroll
-        for (int k = 0; k < HC; ++k) x[k] = __fmul_rn(x[k], inv);
-      }
-    }
+  auto cols = [&]() {
 #pragma unroll
     for (int k = 0; k < HC; ++k) {
       const float inv = rcp_fast(__fadd_rn(sum4_paired(c[k], c[HC + k], c[2 * HC + k], c[3 * HC + k]), eps));
 #pragma unroll
       for (int r = 0; r < HC; ++r) c[HC * r + k] = __fmul_rn(c[HC * r + k], inv);
     }
+  };
+  // round 1: columns; rounds 2 .. repeat: rows, then columns
+  cols();
+#pragma unroll 4
+  for (int it = 1; it < p.repeat; ++it) {
+#pragma unroll
+    for (int r = 0; r < HC; ++r) {
+      float *x = c + HC * r;
+      const float inv = rcp_fast(__fadd_rn(sum4_paired(x[0], x[1], x[2], x[3]), eps));
+#pragma unroll
+      for (int k = 0; k < HC; ++k) x[k] = __fmul_rn(x[k], inv);
+    }
+    cols();
   }
   float *dst = p.comb_out + (size_t)t * HC * HC;
 #pragma unroll
@@ -233,8 +243,11 @@ __device__ __forceinline__ void post_and_sinkhorn16(const MixArgs p, int t, cons
   peak = fmaxf(peak, __shfl_xor_sync(0xffffffffu, peak, 2));
   x = expf(__fsub_rn(x, peak));
   x = __fadd_rn(__fmul_rn(x, rcp_fast(lane_sum4(x, 1))), eps);
-  for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, 1), eps)));
+  // round 1: columns; rounds 2 .. repeat: rows, then columns
+  x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, HC), eps)));
+#pragma unroll 4
+  for (int it = 1; it < p.repeat; ++it) {
+    x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, 1), eps)));
     x = __fmul_rn(x, rcp_fast(__fadd_rn(lane_sum4(x, HC), eps)));
   }
   if (live) p.comb_out[(size_t)t * HC * HC + e] = x;
@@ -267,13 +280,7 @@ __device__ __forceinline__ void post_and_sinkhorn4(const MixArgs p, int t, const
 #pragma unroll
     for (int k = 0; k < HC; ++k) c[k] = __fadd_rn(__fmul_rn(c[k], inv), eps);
   }
-#pragma unroll 1
-  for (int it = 0; it < p.repeat; ++it) {
-    if (it > 0) {
-      const float inv = rcp_fast(__fadd_rn(sum4_paired(c[0], c[1], c[2], c[3]), eps));
-#pragma unroll
-      for (int k = 0; k < HC; ++k) c[k] = __fmul_rn(c[k], inv);
-    }
+  auto cols = [&]() {
     float s[HC];
 #pragma unroll
     for (int k = 0; k < HC; ++k) s[k] = __fadd_rn(c[k], __shfl_xor_sync(0xffffffffu, c[k], 1));
@@ -281,6 +288,15 @@ __device__ __forceinline__ void post_and_sinkhorn4(const MixArgs p, int t, const
     for (int k = 0; k < HC; ++k) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xffffffffu, s[k], 2));
 #pragma unroll
     for (int k = 0; k < HC; ++k) c[k] = __fmul_rn(c[k], rcp_fast(__fadd_rn(s[k], eps)));
+  };
+  // round 1: columns; rounds 2 .. repeat: rows, then columns
+  cols();
+#pragma unroll 4
+  for (int it = 1; it < p.repeat; ++it) {
+    const float inv = rcp_fast(__fadd_rn(sum4_paired(c[0], c[1], c[2], c[3]), eps));
+#pragma unroll
+    for (int k = 0; k < HC; ++k) c[k] = __fmul_rn(c[k], inv);
+    cols();
   }
   if (live) {
     float *dst = p.comb_out + (size_t)t * HC * HC + HC * r;
