@@ -233,8 +233,8 @@ bool side_join_needed(const mhc_boundary *b, unsigned long long capture) {
 // partials a token after any fold or owner reduce), or 0 for the stage and
 // finish kernels: the FP32 weight, and every token's cluster share within the
 // tokens a cluster takes at this shape, all clusters running at once.
-int small_clusters_for(const mhc_boundary *b, int m, int tp, bool fp32_weight) {
-  if (!fp32_weight || b->small_cs == 0 || m > SMALL_M_MAX) return 0;
+int small_clusters_for(const mhc_boundary *b, int m, int tp) {
+  if (b->small_cs == 0 || m > SMALL_M_MAX) return 0;
   const int b_max = small_tokens_max(b->cfg.hidden, tp, b->small_cs);
   const int clusters = m < b->small_clusters ? m : b->small_clusters;
   if (b_max < 1 || clusters < 1 || (m + clusters - 1) / clusters > b_max) return 0;
@@ -291,7 +291,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
   const bool separate = (c.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) != 0;
   const bool on_side = separate && !sync_mixes;
   // a few tokens: the whole boundary in one kernel of CTA clusters
-  const int clusters = small_clusters_for(b, a->m, sp.tp, a->hc_fn != nullptr);
+  const int clusters = small_clusters_for(b, a->m, sp.tp);
   if (clusters > 0) {
     SmallParams q = {};
     q.m = a->m;
@@ -304,6 +304,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     q.post = a->post;
     q.comb = a->comb;
     q.hc_fn = a->hc_fn;
+    q.hc_fn_bf16 = static_cast<const uint16_t *>(a->hc_fn_bf16);
     q.scale = a->scale;
     q.base = a->base;
     q.gamma = static_cast<const uint16_t *>(a->norm_weight);
@@ -867,12 +868,12 @@ size_t mhc_mxfp8_scale_bytes(int32_t m, int32_t hidden) { return scale_bytes(m, 
 
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b) {
   if (!b) return 0;
-  // for a call of max_num_tokens tokens with the FP32 weight: the one-kernel
+  // for a call of max_num_tokens tokens (either weight form): the one-kernel
   // path, or the stage and finish kernels; plus a separate post / Sinkhorn
   // kernel, plus the owner reduce
   const bool owner = (b->cfg.flags & MHC_FLAG_OWNER_REDUCE) != 0;
   const int tp = owner ? 1 : b->cfg.tp;
-  const int core = small_clusters_for(b, b->cfg.max_num_tokens, tp, true) > 0 ? 1 : 2;
+  const int core = small_clusters_for(b, b->cfg.max_num_tokens, tp) > 0 ? 1 : 2;
   return core + ((b->cfg.flags & (MHC_FLAG_SIDE_MIXES | MHC_FLAG_SYNC_MIXES)) ? 1 : 0) + (owner ? 1 : 0);
 }
 

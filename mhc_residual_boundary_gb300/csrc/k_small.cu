@@ -141,7 +141,7 @@ __device__ __forceinline__ float lane4(const float4 &v, int j) {
 }
 
 struct GemvArgs {
-  const float *w;              // the weight rows [4 * cols][24]
+  const void *w;               // the weight rows [4 * cols][24], FP32 or BF16
   const unsigned char *x;      // token 0's new streams [4][cols] bf16; token t at + t * sbytes
   int sbytes, K;               // K = 4 * cols rows
   float *gred;                 // [16 warps][SMALL_B_MAX][24]: each warp's sums
@@ -149,9 +149,10 @@ struct GemvArgs {
 
 // This CTA's part of the GEMV for B tokens: lane l < 30 of warp w takes
 // outputs 4 * (l % 6) .. +3 of rows k = 5 * w + l / 6, + 80, + 160, ... (a warp
-// reads 5 whole 96-byte weight rows, without bank conflicts); each warp's
-// five row lanes of an output quad are summed in order into gred.
-template <int B>
+// reads 5 whole weight rows of 96 (FP32) or 48 (BF16) bytes, without bank
+// conflicts); each warp's five row lanes of an output quad are summed in
+// order into gred.  A BF16 weight widens exactly to FP32.
+template <int B, bool BF16W>
 __device__ __noinline__ void gemv_part(const GemvArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int iq = lane % 6, rr = lane / 6;
@@ -159,9 +160,14 @@ __device__ __noinline__ void gemv_part(const GemvArgs a) {
 #pragma unroll
   for (int t = 0; t < B; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane < 30) {
-    const float *w = a.w + iq * 4;
     for (int k = GEMV_ROWS_WARP * warp + rr; k < a.K; k += GEMV_ROWS_PASS) {
-      const float4 wv = *reinterpret_cast<const float4 *>(w + k * MIX);
+      float4 wv;
+      if (BF16W) {
+        const uint2 q = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.w) + k * MIX + iq * 4);
+        wv = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
+      } else {
+        wv = *reinterpret_cast<const float4 *>(static_cast<const float *>(a.w) + k * MIX + iq * 4);
+      }
 #pragma unroll
       for (int t = 0; t < B; ++t) {
         const float x = __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t *>(a.x + t * a.sbytes + k * 2)) << 16);
@@ -187,6 +193,9 @@ __device__ __noinline__ void gemv_part(const GemvArgs a) {
   }
 }
 
+// One instantiation a weight form, so that the FP32 kernel carries none of
+// the BF16 form's code.
+template <bool BF16W>
 __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem + Ctl::wbar);
@@ -236,16 +245,50 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   cluster_sync();
   pdl_launch_dependents();
 
-  // the weight rows of this CTA's columns (a layer weight: before the wait)
+  // the weight rows of this CTA's columns (a layer weight: before the wait).
+  // FP32 ([4H][24]): stream j's rows are one run, [4 * cols][24] as copied.
+  // BF16 ([GLM] [24][4H]): the 96 row pieces (output i, stream j) are staged
+  // [i][j][cols] in the second half of the weight area, then transposed to
+  // [4 * cols][24] BF16 in the first half.
+  constexpr bool bf16w = BF16W;
+  unsigned char *stg = w_s + weight_bytes(p.cols_max) / 2;
   auto load_weight = [&]() {
     if (warp == 0 && cols > 0) {
-      if (lane == 0) tc::mbar_arrive_expect_tx(wbar, uint32_t(weight_bytes(cols)));
+      if (lane == 0) tc::mbar_arrive_expect_tx(wbar, uint32_t(bf16w ? weight_bytes(cols) / 2 : weight_bytes(cols)));
       __syncwarp();
-      if (lane < HC)
+      if (bf16w) {
+        for (int e = lane; e < MIX * HC; e += 32)
+          tc::bulk_load(stg + e * cols * 2, p.hc_fn_bf16 + (size_t)(e / HC) * HC * H + (size_t)(e % HC) * H + c0,
+                        uint32_t(cols * 2), wbar);
+      } else if (lane < HC) {
         tc::bulk_load(w_s + lane * cols * MIX * 4, p.hc_fn + ((size_t)lane * H + c0) * MIX, uint32_t(cols * MIX * 4), wbar);
+      }
     }
   };
-  if (p.early_weight) load_weight();
+  auto transpose_weight = [&]() {
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(stg);
+    for (int k = tid; k < HC * cols; k += NT) {
+      const int j = k / cols, c = k % cols;
+      uint32_t w[MIX / 2];
+#pragma unroll
+      for (int i2 = 0; i2 < MIX / 2; ++i2)
+        w[i2] = uint32_t(src[((2 * i2) * HC + j) * cols + c]) | (uint32_t(src[((2 * i2 + 1) * HC + j) * cols + c]) << 16);
+      uint4 *d = reinterpret_cast<uint4 *>(w_s + k * MIX * 2);
+      d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      d[2] = make_uint4(w[8], w[9], w[10], w[11]);
+    }
+  };
+  if (p.early_weight) {
+    load_weight();
+    if (bf16w) {
+      // staged and transposed while the kernel ahead finishes
+      if (cols > 0 && !tc::mbar_wait_bounded(wbar, 0u, WAIT_LIMIT)) *bad = 1;
+      __syncthreads();
+      if (*bad == 0) transpose_weight();
+      __syncthreads();
+    }
+  }
   pdl_wait();
   if (!p.early_weight) load_weight();
   // each token's partials, streams, post and comb (lanes of warp 0 issue)
@@ -275,6 +318,10 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   if (b > 0 && !tc::mbar_wait_bounded(dbar, 0u, WAIT_LIMIT)) *bad = 1;
   if (b > 0 && cols > 0 && !tc::mbar_wait_bounded(wbar, 0u, WAIT_LIMIT)) *bad = 1;
   __syncthreads();
+  if (bf16w && !p.early_weight) {
+    if (*bad == 0) transpose_weight();
+    __syncthreads();
+  }
   const bool ok = *bad == 0;
 
   // ---- 2. stage-1 sum and post-mix: item (token, fragment)
@@ -343,16 +390,16 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   // cluster's tokens unrolled for their number)
   float *gred = reinterpret_cast<float *>(smem + Ctl::gred);
   {
-    const GemvArgs ga = {reinterpret_cast<const float *>(w_s), slots + slot_res(tp, cols), sbytes, HC * cols, gred};
+    const GemvArgs ga = {w_s, slots + slot_res(tp, cols), sbytes, HC * cols, gred};
     switch (ok ? b : 0) {
-      case 1: gemv_part<1>(ga); break;
-      case 2: gemv_part<2>(ga); break;
-      case 3: gemv_part<3>(ga); break;
-      case 4: gemv_part<4>(ga); break;
-      case 5: gemv_part<5>(ga); break;
-      case 6: gemv_part<6>(ga); break;
-      case 7: gemv_part<7>(ga); break;
-      case 8: gemv_part<8>(ga); break;
+      case 1: gemv_part<1, BF16W>(ga); break;
+      case 2: gemv_part<2, BF16W>(ga); break;
+      case 3: gemv_part<3, BF16W>(ga); break;
+      case 4: gemv_part<4, BF16W>(ga); break;
+      case 5: gemv_part<5, BF16W>(ga); break;
+      case 6: gemv_part<6, BF16W>(ga); break;
+      case 7: gemv_part<7, BF16W>(ga); break;
+      case 8: gemv_part<8, BF16W>(ga); break;
       default: break;
     }
   }
@@ -569,8 +616,11 @@ int small_tokens_max(int hidden, int tp, int cs) {
 }
 
 cudaError_t small_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(k_small, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(k_small, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaSuccess;
+  for (auto k : {k_small<false>, k_small<true>}) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
   return e;
 }
 
@@ -588,7 +638,7 @@ int small_active_clusters(int cs, size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_small, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, k_small<false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -598,7 +648,8 @@ int small_active_clusters(int cs, size_t smem) {
 cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream) {
   if (p.cs != 8 && p.cs != 16) return cudaErrorInvalidValue;
   const int b_max = small_tokens_max(p.hidden, p.tp, p.cs);
-  if (b_max < 1 || clusters < 1 || (p.m + clusters - 1) / clusters > b_max || !p.hc_fn) return cudaErrorInvalidValue;
+  if (b_max < 1 || clusters < 1 || (p.m + clusters - 1) / clusters > b_max || !p.hc_fn == !p.hc_fn_bf16)
+    return cudaErrorInvalidValue;
   if (p.cols_max != small_cols_max(p.hidden, p.cs)) return cudaErrorInvalidValue;
   const int b = (p.m + clusters - 1) / clusters;
   cudaLaunchConfig_t cfg = {};
@@ -615,7 +666,7 @@ cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k_small, p);
+  return p.hc_fn_bf16 ? cudaLaunchKernelEx(&cfg, k_small<true>, p) : cudaLaunchKernelEx(&cfg, k_small<false>, p);
 }
 
 }  // namespace mhc

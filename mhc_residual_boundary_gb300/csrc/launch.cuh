@@ -92,7 +92,8 @@ struct SmallParams {
   const uint16_t *residual;   // [m][4][H]
   const float *post;          // [m][4]
   const float *comb;          // [m][4][4]
-  const float *hc_fn;         // [4H][24] f32
+  const float *hc_fn;         // [4H][24] f32, or null
+  const uint16_t *hc_fn_bf16; // [24][4H] bf16, or null (exactly one of the two)
   const float *scale;         // [3]
   const float *base;          // [24]
   const uint16_t *gamma;      // [H]

@@ -148,7 +148,8 @@ def test_other_scalars(Boundary):
           norm_eps=1e-2, seed=9)
 
 
-@pytest.mark.parametrize("hidden,tp,m,bf16,moe", [(5120, 4, 4, False, False), (6144, 8, 300, False, False),
+@pytest.mark.parametrize("hidden,tp,m,bf16,moe", [(5120, 4, 4, False, False), (1024, 4, 6, True, False),
+                                                  (6144, 8, 300, False, False),
                                                   (2048, 3, 1024, False, False), (6144, 4, 64, True, False),
                                                   (1024, 4, 60, False, True)])
 def test_static_weight(Boundary, hidden, tp, m, bf16, moe):
