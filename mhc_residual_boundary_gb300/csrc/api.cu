@@ -278,7 +278,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     fo.shared = static_cast<const uint16_t *>(moe->shared);
     fo.y = b->fold;
     fo.err = b->err;
-    e = launch_moe_fold(fo, b->sm_count * 16, stream);
+    e = launch_moe_fold(fo, b->sm_count * 6, stream);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
@@ -452,7 +452,7 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
     fo.shared = static_cast<const uint16_t *>(a->shared);
     fo.y = b->fold;
     fo.err = b->err;
-    e = launch_moe_fold(fo, b->sm_count * 16, stream);
+    e = launch_moe_fold(fo, b->sm_count * 6, stream);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
