@@ -104,6 +104,18 @@ def test_few_tokens(Boundary, hidden, tp, m, bf16):
     check(Boundary, hidden, tp, m, bf16_weight=bf16, mxfp8=hidden % 128 == 0, seed=hidden + 3 * m)
 
 
+@pytest.mark.parametrize("hidden,tp,m,bf16,mxfp8", [(1024, 16, 3, False, True), (512, 32, 1, False, False),
+                                                   (2048, 12, 8, False, True), (4096, 9, 5, False, True),
+                                                   (512, 8, 1, True, False), (776, 3, 6, False, False),
+                                                   (7168, 8, 7, True, True)])
+def test_one_kernel_shapes(Boundary, hidden, tp, m, bf16, mxfp8):
+    # the cluster kernel for a few tokens: many partials a token (tp up to
+    # 32, more than the tensor-core path takes; the BF16 weight is accepted
+    # up to tp = 8), a width that is not a multiple of 32 (16-byte column
+    # units), two tokens a cluster from five tokens, both weight forms
+    check(Boundary, hidden, tp, m, bf16_weight=bf16, mxfp8=mxfp8, seed=hidden * 3 + tp + m)
+
+
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("m", range(1, 10))
 def test_one_to_nine_tokens(Boundary, m, bf16):
