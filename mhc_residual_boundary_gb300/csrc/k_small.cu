@@ -140,6 +140,25 @@ __device__ __forceinline__ float lane4(const float4 &v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
+// Loads from this CTA's shared memory by 32-bit shared-window address: the
+// GEMV below is a separate function, so a generic pointer would reach it
+// without its address space.
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_u2(uint32_t a) {
+  uint2 v;
+  asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short h;
+  asm("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+  return h;
+}
+
 struct GemvArgs {
   const void *w;               // the weight rows [4 * cols][24], FP32 or BF16
   const unsigned char *x;      // token 0's new streams [4][cols] bf16; token t at + t * sbytes
@@ -160,17 +179,18 @@ __device__ __noinline__ void gemv_part(const GemvArgs a) {
 #pragma unroll
   for (int t = 0; t < B; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane < 30) {
+    const uint32_t w0 = tc::smem_addr(a.w) + uint32_t(iq * 4 * (BF16W ? 2 : 4)), x0 = tc::smem_addr(a.x);
     for (int k = GEMV_ROWS_WARP * warp + rr; k < a.K; k += GEMV_ROWS_PASS) {
       float4 wv;
       if (BF16W) {
-        const uint2 q = *reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.w) + k * MIX + iq * 4);
+        const uint2 q = lds_u2(w0 + uint32_t(k * MIX * 2));
         wv = make_float4(bf16_lo(q.x), bf16_hi(q.x), bf16_lo(q.y), bf16_hi(q.y));
       } else {
-        wv = *reinterpret_cast<const float4 *>(static_cast<const float *>(a.w) + k * MIX + iq * 4);
+        wv = lds_f4(w0 + uint32_t(k * MIX * 4));
       }
 #pragma unroll
       for (int t = 0; t < B; ++t) {
-        const float x = __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t *>(a.x + t * a.sbytes + k * 2)) << 16);
+        const float x = __uint_as_float(lds_u16(x0 + uint32_t(t * a.sbytes + k * 2)) << 16);
         acc[t].x = fmaf(wv.x, x, acc[t].x);
         acc[t].y = fmaf(wv.y, x, acc[t].y);
         acc[t].z = fmaf(wv.z, x, acc[t].z);
