@@ -341,6 +341,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     // partial-sum groups: 64-column slices (CUDA-core kernel) or 128-column
     // groups (tensor-core kernel); the scratch holds the larger count
     const bool tc_path = sp.tp <= TP_TMA_MAX;
+    int stage_grid = 0;   // CTAs of the tensor-core stage kernel
     sp.slices = tc_path ? (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS : b->slices;
     sp.residual = static_cast<const uint16_t *>(a->residual);
     sp.post = a->post;
@@ -354,7 +355,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     sp.part = b->part;
     sp.part_stride = part_row_floats(sp.slices);
     sp.err = b->err;
-    e = tc_path ? launch_stage_tc(sp, b->sm_count, stream) : launch_stage(sp, stream);
+    e = tc_path ? launch_stage_tc(sp, b->sm_count, stream, &stage_grid) : launch_stage(sp, stream);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
     if (ev) {
       cudaEventRecord(ev[1], stream);
@@ -385,7 +386,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     fp.layer_input = static_cast<uint16_t *>(a->layer_input);
     fp.mx_values = a->mxfp8_values;
     fp.mx_scales = a->mxfp8_scales;
-    e = launch_finish(fp, b->sm_count, stream, ev == nullptr);
+    e = launch_finish(fp, b->sm_count, stream, ev == nullptr, stage_grid);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
     if (ev) cudaEventRecord(ev[3], stream);
   }
@@ -473,7 +474,8 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
   sp.part = b->part;
   sp.part_stride = part_row_floats(sp.slices);
   sp.err = b->err;
-  e = launch_stage_tc(sp, b->sm_count, stream);
+  int stage_grid = 0;
+  e = launch_stage_tc(sp, b->sm_count, stream, &stage_grid);
   if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
   if (a->pre) {
     FinishParams fp = {};
@@ -489,7 +491,7 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
     fp.mx_values = a->mxfp8_values;
     fp.mx_scales = a->mxfp8_scales;
     fp.err = b->err;
-    e = launch_finish(fp, b->sm_count, stream, true);
+    e = launch_finish(fp, b->sm_count, stream, true, stage_grid);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
   }
   b->last_error.clear();

@@ -73,6 +73,7 @@ __host__ __device__ inline size_t slot_bytes(int hidden, int part_stride) {
 // trades 4 CTAs x 1 slot for 2 x 2, which measured 2 % faster a call at 4096
 // tokens on 152 SMs and 1-2 % slower at 512-1024.
 constexpr int DEEP_TOKENS = 12;
+constexpr int SPREAD_TOKENS = 6;   // see launch_finish
 struct Occupancy {
   int ctas, slots;
 };
@@ -359,12 +360,33 @@ cudaError_t finish_set_attributes() {
   return cudaSuccess;
 }
 
-cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl) {
+cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl, int stage_grid) {
   if (p.hidden % VEC || p.hidden > MAX_HIDDEN || p.part_stride % 4 || p.part_stride < p.slices * VALUES)
     return cudaErrorInvalidValue;
-  const Occupancy occ = occupancy(p.hidden, p.part_stride, p.m >= DEEP_TOKENS * ctas);
+  const bool deep = p.m >= DEEP_TOKENS * ctas;
+  Occupancy occ = occupancy(p.hidden, p.part_stride, deep);
+  // Spread: at most two CTAs an SM (two slots each when they fit), when up to
+  // SPREAD_TOKENS tokens an SM, packed CTAs would leave fewer SMs free than
+  // the stage kernel of the next call needs.  A stage CTA takes a whole SM,
+  // so its CTAs wait for this kernel's CTAs to leave; packed four an SM, the
+  // ones that found no free SM start several us late and end late, while
+  // two an SM delay every stage CTA about alike.  Two an SM also share an
+  // SM's issue slots among fewer post / Sinkhorn chains.  Same box, CUDA
+  // graph of back-to-back calls, us a call (packed -> spread): H = 6144 tp = 4
+  // at M = 96 15.9 -> 14.3, M = 256 22.0 -> 19.9, M = 512 31.3 -> 30.4,
+  // M = 768 40.8 -> 38.2; H = 5120 tp = 8 at M = 256 21.5 -> 20.1; and where
+  // the stage grid fits beside the packed CTAs (H = 5120 tp = 8, M = 128:
+  // 120 CTAs, 120 free SMs) packing stays ahead, 15.7 against 17.1.
+  const size_t slot = slot_bytes(p.hidden, p.part_stride);
+  size_t smem = size_t(occ.slots) * slot;
+  if (!deep && stage_grid > 0 && occ.ctas > 2 && p.m <= SPREAD_TOKENS * ctas &&
+      ctas - (p.m + occ.ctas - 1) / occ.ctas < stage_grid) {
+    occ.ctas = 2;
+    occ.slots = 2 * slot <= SMEM_SM / 2 ? 2 : 1;
+    // a third CTA must not fit beside two
+    smem = SMEM_SM / 2 > size_t(occ.slots) * slot ? SMEM_SM / 2 : size_t(occ.slots) * slot;
+  }
   const int slots = occ.slots;
-  const size_t smem = size_t(slots) * slot_bytes(p.hidden, p.part_stride);
   if (smem > SMEM_LIMIT) return cudaErrorInvalidValue;
   const int nf = (p.hidden / VEC + CT - 1) / CT;
   // persistent: as many CTAs as are resident at once (the runtime's count, so

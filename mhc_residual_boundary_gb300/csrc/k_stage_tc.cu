@@ -729,7 +729,7 @@ cudaError_t stage_tc_set_attributes() {
   return cudaFuncSetAttribute(k_stage_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX);
 }
 
-cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream) {
+cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream, int *grid_out) {
   if (p.tp < 1 || p.tp > TP_TMA_MAX) return cudaErrorInvalidValue;
   if (p.slices != (p.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS) return cudaErrorInvalidValue;
   if (!(p.fn_terms == 3 && p.hc_fn) && !(p.fn_terms == 1 && p.hc_fn_bf16) && p.fn_terms != 0)
@@ -781,6 +781,7 @@ cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream)
       grid = per * p.slices;
     }
   }
+  if (grid_out) *grid_out = grid;
   const size_t smem = size_t(layout_ring(p.fn_terms)) + size_t(ring_slots(p.tp, p.fn_terms)) * slot_bytes(p.tp);
   // programmatic dependent launch: the CTAs' setup (and, for a layer weight,
   // its staging and split) overlaps the end of the preceding kernel

@@ -151,11 +151,15 @@ cudaError_t launch_stage(const StageParams &p, cudaStream_t stream);
 size_t stage_tc_smem_bytes();
 cudaError_t stage_tc_set_attributes();
 cudaError_t stage_tc_stall_copies(int on);   // test hook, see include/mhc_boundary_test.h
-cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream);
+// `grid_out`, if given, receives the number of CTAs launched.
+cudaError_t launch_stage_tc(const StageParams &p, int ctas, cudaStream_t stream, int *grid_out = nullptr);
 // Finish kernel: persistent CTAs (at most `ctas`), programmatic dependent
-// launch after the stage kernel when `pdl`.
+// launch after the stage kernel when `pdl`.  `stage_grid`: the CTAs of the
+// tensor-core stage kernel of this call (0 if another stage kernel ran); a
+// call of the same shape launches that many again next, and the finish
+// kernel's CTAs per SM are chosen with them in mind.
 cudaError_t finish_set_attributes();
-cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl);
+cudaError_t launch_finish(const FinishParams &p, int ctas, cudaStream_t stream, bool pdl, int stage_grid = 0);
 cudaError_t launch_mixes(const MixesParams &p, cudaStream_t stream);
 // The boundary of a few tokens in one kernel: columns a CTA, shared memory,
 // tokens a cluster (0: the shape does not fit), attributes, clusters that

@@ -181,7 +181,8 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   sp.part = part;
   sp.part_stride = part_row_floats(groups);
   sp.err = err;   // a stage-kernel wait that gives up sets bit 1
-  e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream) : launch_stage(sp, stream);
+  int stage_grid = 0;
+  e = tc_path ? launch_stage_tc(sp, g_sm_count[device], stream, &stage_grid) : launch_stage(sp, stream);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "stage kernel: %s", cudaGetErrorString(e));
 
   FinishParams fp = {};
@@ -204,7 +205,7 @@ extern "C" mhc_status_t mhc_boundary_run_static(const mhc_boundary_config_t *con
   fp.layer_input = static_cast<uint16_t *>(a->layer_input);
   fp.mx_values = a->mxfp8_values;
   fp.mx_scales = a->mxfp8_scales;
-  e = launch_finish(fp, g_sm_count[device], stream, true);
+  e = launch_finish(fp, g_sm_count[device], stream, true, stage_grid);
   if (e != cudaSuccess) return report(error, error_len, MHC_ERR_CUDA, "finish kernel: %s", cudaGetErrorString(e));
 
   MixesParams mp = {};
