@@ -99,7 +99,6 @@ constexpr int A_HALF = ROWS * A_ROW;          // 16 KB
 constexpr int A_BYTES = 2 * A_HALF;
 constexpr int B_KCOL = UN * 16;               // bytes between B core columns
 constexpr int TERM_BYTES = KCOLS * B_KCOL;    // one BF16 term of B
-constexpr int B_BYTES = 3 * TERM_BYTES;       // FP32 weight: hi, mid, lo
 constexpr int ROW = UK * 2;                   // bytes of one 128-column BF16 row piece
 constexpr int MAX_SLOTS = 8;
 constexpr uint32_t D_STRIDE = 128;            // TMEM columns between the two accumulators
@@ -208,33 +207,56 @@ __device__ __forceinline__ void add_bf16x2(float2 &acc, uint32_t w) {
 // matrices [term][core column][8-column block][8 columns][8 inputs];
 // column n = stream * 24 + output, input k = column in the group.  Mixer
 // thread `tid` owns element pairs e = tid + 512 * it (inputs 2kp, 2kp + 1 of
-// column n), with (kp, n) chosen so that a warp's 32 stores fill 32 banks.
-__device__ __forceinline__ void b_pair(int e, int &kp, int &n) {
-  const int rest = e >> 5;
-  kp = (rest / 12) * 4 + (e & 3);
-  n = (rest % 12) * 8 + ((e >> 2) & 7);
-}
+// column n), with (kp, n) chosen so that a warp's 32 stores fill 32 banks:
+// with rest = e / 32, kp = 4 (rest / 12) + e % 4 and n = 8 (rest % 12) +
+// (e / 4) % 8.
 
 // Splits the group's staged hc_fn rows (stream j's rows at stg + j * 128 * 24
 // floats; rows past `rows` are treated as zero) into B.  A plain loop: the
-// code is short, and every load is a shared-memory read.
+// code is short, and every load is a shared-memory read.  The operands are
+// addressed through their 32-bit shared-window addresses: this is a separate
+// function, which generic pointers would reach without their address space.
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
 __device__ __noinline__ void convert_b(const float *stg, int rows, unsigned char *b_s) {
+  const uint32_t s0 = tc::smem_addr(stg), b0 = tc::smem_addr(b_s);
+  // Element pair e = tid + 512 * it (above): rest = e / 32 grows by 16 = 12 + 4
+  // an iteration, so its quotient q and remainder r by 12 are carried along;
+  // then kp = 4q + e % 4, n = 8r + c with c = (e / 4) % 8 (fixed), and n's
+  // stream j = r / 3, output i = 8 (r % 3) + c.
+  const int c = (int(threadIdx.x) >> 2) & 7, kq = int(threadIdx.x) & 3;
+  int q = 0, r = int(threadIdx.x) >> 5;   // rest < 16 at it = 0
+  if (r >= 12) {
+    q = 1;
+    r -= 12;
+  }
 #pragma unroll 2
   for (int it = 0; it < B_PAIRS; ++it) {
-    int kp, n;
-    b_pair(threadIdx.x + it * MIX_THREADS, kp, n);
-    const int j = n / MIX, i = n % MIX, k = 2 * kp;
-    const float *src = stg + (j * UK + k) * MIX + i;
-    const float x0 = k < rows ? src[0] : 0.f;
-    const float x1 = k + 1 < rows ? src[MIX] : 0.f;
+    const int kp = 4 * q + kq, k = 2 * kp;
+    const int j = (r * 11) >> 5, i = (r - 3 * j) * 8 + c;   // r / 3 for r < 12
+    const uint32_t src = s0 + uint32_t(((j * UK + k) * MIX + i) * 4);
+    const float x0 = k < rows ? lds_f32(src) : 0.f;
+    const float x1 = k + 1 < rows ? lds_f32(src + MIX * 4) : 0.f;
     const uint32_t hi = pack_bf16x2(x0, x1);
     const float r0 = __fsub_rn(x0, bf16_lo(hi)), r1 = __fsub_rn(x1, bf16_hi(hi));
     const uint32_t mid = pack_bf16x2(r0, r1);
     const uint32_t lo = pack_bf16x2(__fsub_rn(r0, bf16_lo(mid)), __fsub_rn(r1, bf16_hi(mid)));
-    unsigned char *dst = b_s + (kp >> 2) * B_KCOL + (n >> 3) * 128 + (n & 7) * 16 + (kp & 3) * 4;
-    *reinterpret_cast<uint32_t *>(dst) = hi;
-    *reinterpret_cast<uint32_t *>(dst + KCOLS * B_KCOL) = mid;
-    *reinterpret_cast<uint32_t *>(dst + 2 * KCOLS * B_KCOL) = lo;
+    const uint32_t dst = b0 + uint32_t(q * B_KCOL + r * 128 + c * 16 + kq * 4);
+    sts_u32(dst, hi);
+    sts_u32(dst + KCOLS * B_KCOL, mid);
+    sts_u32(dst + 2 * KCOLS * B_KCOL, lo);
+    q += 1;
+    r += 4;
+    if (r >= 12) {
+      q += 1;
+      r -= 12;
+    }
   }
 }
 
@@ -443,17 +465,24 @@ __global__ void __launch_bounds__(NT, 1)
   // groups -- group g gets CTAs floor(g * C / G) .. floor((g + 1) * C / G) - 1
   // -- and each takes a contiguous share of its group's tiles, so that no CTA
   // splits a second weight group.
+  // (32-bit unsigned divisions where the products fit, as they do at every
+  // size but a million tokens and more: a 64-bit division by a run-time
+  // value is a long software routine, and this is on every CTA's start)
   int u_begin, u_end;
+  const unsigned C = gridDim.x, b = blockIdx.x;
   if (p.group_aligned) {
-    const long long G = p.slices, C = gridDim.x;
-    const int g = int(((long long)(blockIdx.x + 1) * G - 1) / C);
-    const int c0 = int(g * C / G), c1 = int((g + 1) * C / G);
-    const int k = int(blockIdx.x) - c0, n = c1 - c0;
-    u_begin = g * n_tiles + int((long long)k * n_tiles / n);
-    u_end = g * n_tiles + int((long long)(k + 1) * n_tiles / n);
+    const unsigned G = unsigned(p.slices), T = unsigned(n_tiles);
+    const unsigned g = ((b + 1) * G - 1) / C;   // G, C <= 1024
+    const unsigned c0 = g * C / G, c1 = (g + 1) * C / G;
+    const unsigned k = b - c0, n = c1 - c0;
+    const bool narrow = T <= 0xffffffffu / C;
+    u_begin = int(g * T + (narrow ? k * T / n : unsigned((unsigned long long)k * T / n)));
+    u_end = int(g * T + (narrow ? (k + 1) * T / n : unsigned((unsigned long long)(k + 1) * T / n)));
   } else {
-    u_begin = int((long long)blockIdx.x * units / gridDim.x);
-    u_end = int((long long)(blockIdx.x + 1) * units / gridDim.x);
+    const unsigned U = unsigned(units);
+    const bool narrow = U <= 0xffffffffu / C;
+    u_begin = int(narrow ? b * U / C : unsigned((unsigned long long)b * U / C));
+    u_end = int(narrow ? (b + 1) * U / C : unsigned((unsigned long long)(b + 1) * U / C));
   }
   const int n_units = u_end - u_begin;             // >= 1: the grid is at most `units`
   const int nslot = ring_slots(p.tp, p.fn_terms), sbytes = slot_bytes(p.tp);
