@@ -77,7 +77,8 @@ struct Ctl {
   static constexpr int mix = ir + SMALL_B_MAX * 4;               // f32 [SMALL_B_MAX][24]
   static constexpr int item_ss = mix + SMALL_B_MAX * MIX * 4;    // f32 [SMALL_ITEMS_MAX]
   static constexpr int gred = item_ss + SMALL_ITEMS_MAX * 4;     // f32 [16 warps][SMALL_B_MAX][24]: the warps' GEMV sums
-  static constexpr int bad = gred + NWARP * SMALL_B_MAX * MIX * 4; // int: a copy wait gave up
+  static constexpr int sb = gred + NWARP * SMALL_B_MAX * MIX * 4;  // f32 [28]: scale[3], base[24]
+  static constexpr int bad = sb + 28 * 4;                          // int: a copy wait gave up
   static constexpr int end = (bad + 4 + 127) / 128 * 128;
 };
 
@@ -91,8 +92,8 @@ __host__ __device__ constexpr int slot_bytes(int tp, int cols) { return (slot_po
 // Column range of cluster rank r (whole units of `unit` columns).
 __device__ __forceinline__ void col_range(int hidden, int cs, int r, int &c0, int &c1) {
   const int unit = hidden % 32 == 0 ? 32 : VEC, n = hidden / unit;
-  c0 = int((long long)r * n / cs) * unit;
-  c1 = int((long long)(r + 1) * n / cs) * unit;
+  c0 = (r * n / cs) * unit;   // r < 16 and n <= 2048: no overflow
+  c1 = ((r + 1) * n / cs) * unit;
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -311,6 +312,10 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   }
   pdl_wait();
   if (!p.early_weight) load_weight();
+  // scale and base into shared memory now, beside the token's copies: pre and
+  // the post / Sinkhorn warp would otherwise wait on an L2 round trip for them
+  float *sb_s = reinterpret_cast<float *>(smem + Ctl::sb);
+  if (warp == 1 && lane < 3 + MIX) sb_s[lane] = lane < 3 ? p.scale[lane] : p.base[lane - 3];
   // each token's partials, streams, post and comb (lanes of warp 0 issue)
   const bool stall = *static_cast<volatile int *>(&g_stall_copies) != 0;
   if (warp == 0 && b > 0 && !stall) {
@@ -461,8 +466,12 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   if (b > 0 && !tc::mbar_wait_bounded(ibar1, 0u, WAIT_LIMIT)) *bad = 1;
   if (warp < b) {
     float v = 0.f;
-    if (lane < VALUES)
-      for (int r = 0; r < cs; ++r) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + warp) * IN1_STRIDE + lane]);
+    // (a compile-time bound, so that the 16 loads issue before the adds)
+    if (lane < VALUES) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + warp) * IN1_STRIDE + lane]);
+    }
     const int t = t0 + warp;
     const float ss = __shfl_sync(0xffffffffu, v, MIX);
     const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
@@ -474,7 +483,7 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
       if (mine && p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
     }
     if (lane < HC) {
-      const float pr = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, p.scale[0]), p.base[lane])), p.hc_eps);
+      const float pr = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, sb_s[0]), sb_s[3 + lane])), p.hc_eps);
       pre_s[warp * HC + lane] = pr;
       if (mine && p.pre_out) p.pre_out[(size_t)t * HC + lane] = pr;
     }
@@ -491,7 +500,7 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     if (p.post_out) {
       // tokens t of this cluster with t % cs == rank, one a quad of lanes
       const int first = (int(rank) - t0 % cs + cs) % cs;   // first local index with (t0 + i) % cs == rank
-      const MixArgs ma = {p.scale, p.base, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
+      const MixArgs ma = {sb_s, sb_s + 3, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
       for (int i0 = first; i0 < b; i0 += 8 * cs) {
         const int i = i0 + (lane >> 2) * cs;
         const bool live = ok && i < b;
@@ -558,7 +567,9 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     if (b > 0 && !tc::mbar_wait_bounded(ibar2, 0u, WAIT_LIMIT)) *bad = 1;
     if (warp < b && lane == 0) {
       float s = 0.f;
-      for (int r = 0; r < cs; ++r) s = __fadd_rn(s, inbox2[r * 8 + warp]);
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        if (r < cs) s = __fadd_rn(s, inbox2[r * 8 + warp]);
       ir_s[warp] = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(s, float(H)), p.norm_eps)));
     }
     item_sync();
