@@ -55,6 +55,7 @@ __device__ int g_stall_copies = 0;
 constexpr int NT = 512;
 constexpr int NWARP = NT / 32;
 constexpr int SINK_WARP = NWARP - 1;           // post / Sinkhorn, no collapse items
+static_assert(SMALL_B_MAX <= 8, "a CTA owns at most one token's post / Sinkhorn (clusters of 8 or 16)");
 constexpr int ITEM_THREADS = NT - 32;          // threads of the collapse and normalisation items
 constexpr int GEMV_ROWS_WARP = 5;              // weight rows a warp takes at once (30 lanes)
 constexpr int GEMV_ROWS_PASS = GEMV_ROWS_WARP * NWARP;   // 80
@@ -78,7 +79,8 @@ struct Ctl {
   static constexpr int item_ss = mix + SMALL_B_MAX * MIX * 4;    // f32 [SMALL_ITEMS_MAX]
   static constexpr int gred = item_ss + SMALL_ITEMS_MAX * 4;     // f32 [16 warps][SMALL_B_MAX][24]: the warps' GEMV sums
   static constexpr int sb = gred + NWARP * SMALL_B_MAX * MIX * 4;  // f32 [28]: scale[3], base[24]
-  static constexpr int bad = sb + 28 * 4;                          // int: a copy wait gave up
+  static constexpr int smix = sb + 28 * 4;                         // f32 [24]: the post / Sinkhorn token's mixes
+  static constexpr int bad = smix + MIX * 4;                       // int: a copy wait gave up
   static constexpr int end = (bad + 4 + 127) / 128 * 128;
 };
 
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   // scale and base into shared memory now, beside the token's copies: pre and
   // the post / Sinkhorn warp would otherwise wait on an L2 round trip for them
   float *sb_s = reinterpret_cast<float *>(smem + Ctl::sb);
+  float *smix_s = reinterpret_cast<float *>(smem + Ctl::smix);
   if (warp == 1 && lane < 3 + MIX) sb_s[lane] = lane < 3 ? p.scale[lane] : p.base[lane - 3];
   // each token's partials, streams, post and comb (lanes of warp 0 issue)
   const bool stall = *static_cast<volatile int *>(&g_stall_copies) != 0;
@@ -487,8 +490,27 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
       pre_s[warp * HC + lane] = pr;
       if (mine && p.pre_out) p.pre_out[(size_t)t * HC + lane] = pr;
     }
+  } else if (warp == SINK_WARP && p.post_out) {
+    // The post / Sinkhorn warp computes the mixes of its token itself (the
+    // same operations as above, so the same bits) and starts at once, not
+    // after the barrier below: its chain is the longest of the call.  A CTA
+    // has at most one such token (b <= 8 <= cs).
+    const int first = (int(rank) - t0 % cs + cs) % cs;
+    if (first < b) {
+      float v = 0.f;
+      if (lane < VALUES) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + first) * IN1_STRIDE + lane]);
+      }
+      const float ss = __shfl_sync(0xffffffffu, v, MIX);
+      const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
+      if (lane < MIX) smix_s[lane] = __fmul_rn(v, rstd);
+    }
+    __syncwarp();
   }
-  __syncthreads();
+  // the collapse needs every token's pre; the post / Sinkhorn warp goes on
+  if (warp != SINK_WARP) item_sync();
 
   // ---- 5. collapse of this CTA's columns (kept in registers for step 7);
   // meanwhile the last warp runs post and the Sinkhorn mix of this CTA's
@@ -498,13 +520,14 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   if (warp == SINK_WARP) {
     cluster_arrive_relaxed();
     if (p.post_out) {
-      // tokens t of this cluster with t % cs == rank, one a quad of lanes
-      const int first = (int(rank) - t0 % cs + cs) % cs;   // first local index with (t0 + i) % cs == rank
+      // the token t of this cluster with t % cs == rank (first < b), on the
+      // first quad of lanes; the other quads compute on the same mixes and
+      // store nothing
+      const int first = (int(rank) - t0 % cs + cs) % cs;   // local index with (t0 + i) % cs == rank
       const MixArgs ma = {sb_s, sb_s + 3, p.post_out, p.comb_out, p.post_mult, p.hc_eps, p.repeat};
-      for (int i0 = first; i0 < b; i0 += 8 * cs) {
-        const int i = i0 + (lane >> 2) * cs;
-        const bool live = ok && i < b;
-        post_and_sinkhorn4(ma, t0 + (live ? i : 0), mix_s + (live ? i : 0) * MIX, live);
+      if (first < b) {
+        const bool live = ok && lane < 4;
+        post_and_sinkhorn4(ma, t0 + first, smix_s, live);
       }
     }
   } else {
