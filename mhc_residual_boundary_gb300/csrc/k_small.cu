@@ -352,65 +352,78 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   }
   const bool ok = *bad == 0;
 
-  // ---- 2. stage-1 sum and post-mix: item (token, fragment)
+  // ---- 2. stage-1 sum and post-mix: item (token, fragment), four threads an
+  // item (a quad of lanes), thread j of the quad computing new stream j; the
+  // stage-1 sum is computed by all four (the same bits), thread 0 stores it
   const int n_items = b * F;
-  for (int item = tid; ok && item < n_items; item += NT) {
-    const int tl = item / F, f = item % F, t = t0 + tl;
+  for (int base = warp * 32; base < n_items * HC; base += NT) {
+    const int q = base + lane, item = q >> 2, j = q & 3;
+    const bool act = ok && item < n_items;
+    const int tl = act ? item / F : 0, f = act ? item % F : 0, t = t0 + tl;
     unsigned char *st = slots + tl * sbytes;
+    unsigned char *rs = st + slot_res(tp, cols) + f * 16;
     float2 y[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
-    for (int r = 0; r < tp; ++r) {
-      const uint4 w = *reinterpret_cast<const uint4 *>(st + r * cols * 2 + f * 16);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    uint4 res[HC];
+    float pj = 0.f;
+    float ck[HC];
+    if (act) {
+      for (int r = 0; r < tp; ++r) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(st + r * cols * 2 + f * 16);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        y[e].x = __fadd_rn(y[e].x, bf16_lo(ww[e]));
-        y[e].y = __fadd_rn(y[e].y, bf16_hi(ww[e]));
+        for (int e = 0; e < 4; ++e) {
+          y[e].x = __fadd_rn(y[e].x, bf16_lo(ww[e]));
+          y[e].y = __fadd_rn(y[e].y, bf16_hi(ww[e]));
+        }
       }
+#pragma unroll
+      for (int k = 0; k < HC; ++k) res[k] = *reinterpret_cast<const uint4 *>(rs + k * cols * 2);
+      const float *pc = reinterpret_cast<const float *>(st + slot_post(tp, cols));
+      pj = pc[j];
+#pragma unroll
+      for (int k = 0; k < HC; ++k) ck[k] = pc[4 + k * HC + j];   // comb[k][j]
     }
     const uint4 yb = make_uint4(pack_bf16x2(y[0].x, y[0].y), pack_bf16x2(y[1].x, y[1].y),
                                 pack_bf16x2(y[2].x, y[2].y), pack_bf16x2(y[3].x, y[3].y));
     const uint32_t ybw[4] = {yb.x, yb.y, yb.z, yb.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = bf16_pair(ybw[e]);
-    if (p.reduced_out) st_vec(p.reduced_out + (size_t)t * H + c0 + f * VEC, yb);
-    unsigned char *rs = st + slot_res(tp, cols) + f * 16;
-    uint4 res[HC];
+    if (act && j == 0 && p.reduced_out) st_vec(p.reduced_out + (size_t)t * H + c0 + f * VEC, yb);
+    // new_j = y * post_j + sum_k res_k * comb[k][j], one fused multiply-add a
+    // source in source order, on FP32 element pairs
+    float2 o[4];
 #pragma unroll
-    for (int k = 0; k < HC; ++k) res[k] = *reinterpret_cast<const uint4 *>(rs + k * cols * 2);
-    const float4 post = *reinterpret_cast<const float4 *>(st + slot_post(tp, cols));
-    float4 comb[HC];
+    for (int e = 0; e < 4; ++e) o[e] = __fmul2_rn(y[e], dup(pj));
 #pragma unroll
-    for (int k = 0; k < HC; ++k) comb[k] = *reinterpret_cast<const float4 *>(st + slot_post(tp, cols) + 16 + k * 16);
+    for (int k = 0; k < HC; ++k) {
+      const uint32_t ww[4] = {res[k].x, res[k].y, res[k].z, res[k].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = __ffma2_rn(bf16_pair(ww[e]), dup(ck[k]), o[e]);
+    }
+    const uint4 nv = make_uint4(pack_bf16x2(o[0].x, o[0].y), pack_bf16x2(o[1].x, o[1].y),
+                                pack_bf16x2(o[2].x, o[2].y), pack_bf16x2(o[3].x, o[3].y));
+    const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
     float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < HC; ++j) {
-      const float2 pj = dup(lane4(post, j));
-      float2 o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[e] = __fmul2_rn(y[e], pj);
-#pragma unroll
-      for (int k = 0; k < HC; ++k) {
-        const float2 ck = dup(lane4(comb[k], j));
-        const uint32_t ww[4] = {res[k].x, res[k].y, res[k].z, res[k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[e] = __ffma2_rn(bf16_pair(ww[e]), ck, o[e]);
-      }
-      const uint4 nv = make_uint4(pack_bf16x2(o[0].x, o[0].y), pack_bf16x2(o[1].x, o[1].y),
-                                  pack_bf16x2(o[2].x, o[2].y), pack_bf16x2(o[3].x, o[3].y));
-      const uint32_t nw[4] = {nv.x, nv.y, nv.z, nv.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 r2 = bf16_pair(nw[e]);
-        ss2 = __ffma2_rn(r2, r2, ss2);
-      }
-      // the new stream replaces the source stream in the slot (each item owns
-      // its 16 bytes of every stream)
+    for (int e = 0; e < 4; ++e) {
+      const float2 r2 = bf16_pair(nw[e]);
+      ss2 = __ffma2_rn(r2, r2, ss2);
+    }
+    // the item's sum of squares over its four streams: ((s0 + s1) + (s2 + s3))
+    float s4 = act ? __fadd_rn(ss2.x, ss2.y) : 0.f;
+    s4 = __fadd_rn(s4, __shfl_xor_sync(0xffffffffu, s4, 1));
+    s4 = __fadd_rn(s4, __shfl_xor_sync(0xffffffffu, s4, 2));
+    // every thread of the quad has read the source streams before any of
+    // them is replaced: the new stream j takes source stream j's place in the
+    // slot (each item owns its 16 bytes of every stream)
+    __syncwarp();
+    if (act) {
       *reinterpret_cast<uint4 *>(rs + j * cols * 2) = nv;
       st_vec(p.residual_out + ((size_t)t * HC + j) * H + c0 + f * VEC, nv);
+      if (j == 0) item_ss[item] = s4;
     }
-    item_ss[item] = __fadd_rn(ss2.x, ss2.y);
   }
   __syncthreads();
 
