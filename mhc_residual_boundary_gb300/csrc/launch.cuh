@@ -80,10 +80,13 @@ struct FinishParams {
 constexpr int SMALL_B_MAX = 8;
 constexpr int SMALL_ITEMS_MAX = 512;   // (token, 16-byte fragment) items of a CTA
 // Largest call the one-kernel path takes (larger calls run the stage and
-// finish kernels).  Beyond eight tokens its clusters hold most of the SMs, so
-// the next call's CTAs cannot start their prologue beside it, and the stage
-// and finish kernels are as fast (measured at H = 5120-7168, tp = 4 and 8).
-constexpr int SMALL_M_MAX = 8;
+// finish kernels).  Up to twelve tokens it takes six or fewer clusters and is
+// the faster path (two tokens a cluster: at H = 6144 tp = 4, 9.1 / 9.3 us a
+// call at 10 / 12 tokens against 10.1 for the stage and finish kernels);
+// from 16 tokens on its clusters hold most of the SMs, so the next call's
+// CTAs cannot start their prologue beside it, and the two kernels are faster
+// (10.1 against 10.8 us at 16 tokens; the same at H = 5120 tp = 8).
+constexpr int SMALL_M_MAX = 12;
 struct SmallParams {
   int m, hidden, tp;
   int cs;                     // CTAs a cluster (8 or 16)

@@ -124,6 +124,15 @@ def test_one_to_nine_tokens(Boundary, m, bf16):
     check(Boundary, 6144, 4, m, bf16_weight=bf16, mxfp8=True, seed=31 * m + bf16)
 
 
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("hidden,tp,m", [(6144, 4, 10), (6144, 4, 12), (6144, 4, 13), (5120, 8, 11), (776, 3, 12)])
+def test_ten_to_thirteen_tokens(Boundary, hidden, tp, m, bf16):
+    # the top of the one-kernel path's range (two tokens a cluster, up to 12
+    # tokens, an odd count leaving a cluster one token) and the stage and
+    # finish kernels just beyond it
+    check(Boundary, hidden, tp, m, bf16_weight=bf16, mxfp8=hidden % 128 == 0, seed=17 * m + hidden + bf16)
+
+
 @pytest.mark.parametrize("hidden,tp,m,bf16", [(2048, 6, 1024, False), (2048, 3, 1024, False),
                                               (6144, 8, 512, True), (2048, 8, 1024, True),
                                               (5120, 8, 2000, False)])
