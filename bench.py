@@ -583,7 +583,8 @@ def measure_workload(w, steps, warmup, device, peak, l2, profile=True, latency=F
 
 
 # Workloads reported beside the headline one in every bench line: (name, M)
-PER_CONFIG = [("tiny", 4), ("decode", 64), ("glm", 1), ("glm", 256), ("glm", 512), ("moe", 256)]
+PER_CONFIG = [("tiny", 4), ("decode", 64), ("glm", 1), ("glm", 8), ("glm", 12), ("glm", 256), ("glm", 512),
+              ("moe", 256)]
 
 
 def per_config(device, peak, l2, steps=2000):
