@@ -279,7 +279,7 @@ mhc_status_t launch_call(mhc_boundary *b, const mhc_run_args_t *a, const mhc_moe
     fo.shared = static_cast<const uint16_t *>(moe->shared);
     fo.y = b->fold;
     fo.err = b->err;
-    e = launch_moe_fold(fo, b->sm_count * 6, stream);
+    e = launch_moe_fold(fo, b->sm_count, stream);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
@@ -454,7 +454,7 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
     fo.shared = static_cast<const uint16_t *>(a->shared);
     fo.y = b->fold;
     fo.err = b->err;
-    e = launch_moe_fold(fo, b->sm_count * 6, stream);
+    e = launch_moe_fold(fo, b->sm_count, stream);
     if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "MoE fold kernel: %s", cudaGetErrorString(e));
     sp.tp = 1;
     sp.partials = b->fold;
@@ -604,6 +604,7 @@ mhc_status_t mhc_boundary_create(const mhc_boundary_config_t *config, int device
   if (e == cudaSuccess) e = stage_tc_set_attributes();
   if (e == cudaSuccess) e = finish_set_attributes();
   if (e == cudaSuccess) e = small_set_attributes();
+  if (e == cudaSuccess) e = moe_fold_set_attributes();
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&b->sm_count, cudaDevAttrMultiProcessorCount, device);
   if (e == cudaSuccess) {
     // the one-kernel path: 16-CTA clusters where they fit at this shape, else 8

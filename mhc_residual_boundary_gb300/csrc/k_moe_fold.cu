@@ -12,11 +12,13 @@
 // An index outside [-1, rows) sets bit 0 of the error word and is treated as
 // a route not held.
 //
-// Layout: CTAs of 8 warps, grid-stride over (token, 256-column chunk) jobs.
-// Lane l of every warp takes the chunk's 16-byte fragment l, so that a warp
-// reads 512 contiguous bytes of a route row; warp w folds ranks w, w + 8, ...,
-// loading a rank's routes four at a time before their multiply-adds.
-// The folded x_r go to shared memory, and warp 0 adds them in rank order.
+// Layout: CTAs of 8 warps, three to an SM, grid-stride over (token,
+// 1024-column chunk) jobs.  Lane l of every warp takes the chunk's 16-byte
+// fragments l, l + 32, l + 64 and l + 96, so that a warp reads 2 KB of a
+// route row in four 512-byte runs, with eight loads of two routes in flight
+// a lane; warp w folds ranks w, w + 8, ...  The folded x_r, already rounded
+// to BF16, go to shared memory (2 KB a rank), and warps 0-3 add them in rank
+// order, a fragment a lane.
 //
 // Page: [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
 #include "device_common.cuh"
@@ -27,81 +29,93 @@ namespace {
 
 constexpr int WARPS = 8;
 constexpr int NT = WARPS * 32;
-constexpr int KB = 4;                        // routes loaded per batch
+constexpr int KB = 2;                        // routes loaded per batch
+constexpr int FR = 4;                        // 16-byte fragments a lane, 512 bytes apart
+constexpr int CHUNK = 32 * FR;               // fragments a job (2 KB of a route row)
 constexpr int TP_MAX = 32;
 
-// Four routes a batch and six CTAs an SM (40 registers a thread, 24 bytes
-// spilled): more warps with gathers in flight than eight routes at four CTAs,
-// measured 4 % faster a MoE call at 256 tokens; eight routes at six CTAs
-// spill 268 bytes and ran 27 % slower.
-__global__ void __launch_bounds__(NT, 6) k_moe_fold(const FoldParams p) {
-  extern __shared__ float4 xs[];             // [tp][32][2]: x_r of the chunk's 32 fragments
+__global__ void __launch_bounds__(NT, 3) k_moe_fold(const FoldParams p) {
+  extern __shared__ uint4 xs[];              // [tp][CHUNK]: x_r of the chunk's fragments, BF16 (rounded already)
   const int H = p.hidden, K = p.top_k, nfrag = H / VEC;
   const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
-  const int chunks = (nfrag + 31) / 32;
+  const int chunks = (nfrag + CHUNK - 1) / CHUNK;
   for (int job = blockIdx.x; job < p.m * chunks; job += gridDim.x) {
-    const int t = job / chunks, fr = (job % chunks) * 32 + lane;
-    const bool live = fr < nfrag;
+    const int t = job / chunks, fr0 = (job % chunks) * CHUNK + lane;
 #pragma unroll 1
     for (int r = warp; r < p.tp; r += WARPS) {
-      float x[8];
+      float x[FR][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      if (live) {
-        // the shared expert's row does not depend on the route indices: its
-        // load is in flight with theirs and the routes'
-        const uint4 sv = ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)fr * VEC);
-        const int32_t *ix = p.idx + ((size_t)r * p.m + t) * K;
-        const float *wt = p.weights + (size_t)t * K;
-        const uint16_t *rows = p.routed + (size_t)r * p.rows_per_rank * H + (size_t)fr * VEC;
+      for (int g = 0; g < FR; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[g][e] = 0.f;
+      // the shared expert's rows do not depend on the route indices: their
+      // loads are in flight with theirs and the routes'
+      uint4 sv[FR];
+#pragma unroll
+      for (int g = 0; g < FR; ++g)
+        sv[g] = fr0 + 32 * g < nfrag ? ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)(fr0 + 32 * g) * VEC)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+      const int32_t *ix = p.idx + ((size_t)r * p.m + t) * K;
+      const float *wt = p.weights + (size_t)t * K;
+      const uint16_t *rows = p.routed + (size_t)r * p.rows_per_rank * H + (size_t)fr0 * VEC;
 #pragma unroll 1
-        for (int k0 = 0; k0 < K; k0 += KB) {
-          int row[KB];
-          uint4 v[KB];
+      for (int k0 = 0; k0 < K; k0 += KB) {
+        int row[KB];
+        uint4 v[KB][FR];
 #pragma unroll
-          for (int i = 0; i < KB; ++i) {
-            row[i] = k0 + i < K ? ix[k0 + i] : -1;
-            if (row[i] < -1 || row[i] >= p.rows_per_rank) {
-              atomicOr(p.err, 1u);
-              row[i] = -1;
-            }
-            v[i] = row[i] >= 0 ? ld_stream(rows + (size_t)row[i] * H) : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < KB; ++i) {
+          row[i] = k0 + i < K ? ix[k0 + i] : -1;
+          if (row[i] < -1 || row[i] >= p.rows_per_rank) {
+            atomicOr(p.err, 1u);
+            row[i] = -1;
           }
 #pragma unroll
-          for (int i = 0; i < KB; ++i) {
-            if (row[i] >= 0) {
-              float a[8];
-              unpack8(v[i], a);
-              const float w = wt[k0 + i];
+          for (int g = 0; g < FR; ++g)
+            v[i][g] = row[i] >= 0 && fr0 + 32 * g < nfrag ? ld_stream(rows + (size_t)row[i] * H + 32 * g * VEC)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = __fmaf_rn(a[e], w, x[e]);
+        for (int i = 0; i < KB; ++i) {
+          if (row[i] >= 0) {
+            const float w = wt[k0 + i];
+#pragma unroll
+            for (int g = 0; g < FR; ++g) {
+              float a[8];
+              unpack8(v[i][g], a);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[g][e] = __fmaf_rn(a[e], w, x[g][e]);
             }
           }
         }
-        float s[8];
-        unpack8(sv, s);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = __fadd_rn(x[e], s[e]);
-        round8(x);
       }
-      xs[(r * 32 + lane) * 2] = make_float4(x[0], x[1], x[2], x[3]);
-      xs[(r * 32 + lane) * 2 + 1] = make_float4(x[4], x[5], x[6], x[7]);
+#pragma unroll
+      for (int g = 0; g < FR; ++g) {
+        if (fr0 + 32 * g < nfrag) {
+          float s[8];
+          unpack8(sv[g], s);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[g][e] = __fadd_rn(x[g][e], s[e]);
+          round8(x[g]);
+        }
+        xs[r * CHUNK + 32 * g + lane] = make_uint4(pack_bf16x2(x[g][0], x[g][1]), pack_bf16x2(x[g][2], x[g][3]),
+                                                   pack_bf16x2(x[g][4], x[g][5]), pack_bf16x2(x[g][6], x[g][7]));
+      }
     }
     __syncthreads();
-    if (warp == 0 && live) {
-      // y = bf16(((0 + x_0) + x_1) + ...)
+    // y = bf16(((0 + x_0) + x_1) + ...): warps 0 .. FR - 1 take a fragment each
+    if (warp < FR && fr0 + 32 * warp < nfrag) {
+      const int fi = 32 * warp + lane;
       float y[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] = 0.f;
 #pragma unroll 1
       for (int r = 0; r < p.tp; ++r) {
-        const float4 a = xs[(r * 32 + lane) * 2], b = xs[(r * 32 + lane) * 2 + 1];
-        y[0] = __fadd_rn(y[0], a.x); y[1] = __fadd_rn(y[1], a.y);
-        y[2] = __fadd_rn(y[2], a.z); y[3] = __fadd_rn(y[3], a.w);
-        y[4] = __fadd_rn(y[4], b.x); y[5] = __fadd_rn(y[5], b.y);
-        y[6] = __fadd_rn(y[6], b.z); y[7] = __fadd_rn(y[7], b.w);
+        float a[8];
+        unpack8(xs[r * CHUNK + fi], a);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __fadd_rn(y[e], a[e]);
       }
-      st_vec(p.y + (size_t)t * H + (size_t)fr * VEC, round8(y));
+      st_vec(p.y + (size_t)t * H + (size_t)(fr0 + 32 * warp) * VEC, round8(y));
     }
     __syncthreads();   // the next job's x_r overwrite these
   }
@@ -109,11 +123,18 @@ __global__ void __launch_bounds__(NT, 6) k_moe_fold(const FoldParams p) {
 
 }  // namespace
 
-cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream) {
+// The rank buffer: tp x CHUNK fragments x 16 bytes.
+cudaError_t moe_fold_set_attributes() {
+  return cudaFuncSetAttribute(k_moe_fold, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TP_MAX * CHUNK * int(sizeof(uint4)));
+}
+
+cudaError_t launch_moe_fold(const FoldParams &p, int sms, cudaStream_t stream) {
+  const int ctas = sms * 3;   // the CTAs resident at once (launch bounds)
   if (p.tp < 1 || p.tp > TP_MAX || p.top_k < 1 || p.top_k > 64 || p.hidden % VEC) return cudaErrorInvalidValue;
-  const int jobs = p.m * ((p.hidden / VEC + 31) / 32);
+  const int jobs = p.m * ((p.hidden / VEC + CHUNK - 1) / CHUNK);
   const int grid = jobs < ctas ? jobs : ctas;
-  k_moe_fold<<<grid, NT, size_t(p.tp) * 32 * 2 * sizeof(float4), stream>>>(p);
+  k_moe_fold<<<grid, NT, size_t(p.tp) * CHUNK * sizeof(uint4), stream>>>(p);
   return cudaGetLastError();
 }
 

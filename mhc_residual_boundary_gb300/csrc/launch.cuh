@@ -174,8 +174,10 @@ cudaError_t small_set_attributes();
 cudaError_t small_stall_copies(int on);   // test hook, see include/mhc_boundary_test.h
 int small_active_clusters(int cs, size_t smem);
 cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream);
-// MoE fold over at most `ctas` CTAs of 128 threads.
-cudaError_t launch_moe_fold(const FoldParams &p, int ctas, cudaStream_t stream);
+// MoE fold: CTAs of 256 threads, at most three for each of the GPU's `sms`
+// SMs; the attributes allow its rank buffer of up to 64 KB.
+cudaError_t moe_fold_set_attributes();
+cudaError_t launch_moe_fold(const FoldParams &p, int sms, cudaStream_t stream);
 cudaError_t launch_owner_reduce(const OwnerParams &p, int ctas, cudaStream_t stream);
 
 }  // namespace mhc
