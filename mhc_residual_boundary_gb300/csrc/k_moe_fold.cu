@@ -18,7 +18,8 @@
 // route row in four 512-byte runs, with eight loads of two routes in flight
 // a lane; warp w folds ranks w, w + 8, ...  The folded x_r, already rounded
 // to BF16, go to shared memory (2 KB a rank), and warps 0-3 add them in rank
-// order, a fragment a lane.
+// order, a fragment a lane.  Every CTA lets the stage kernel's launch begin at
+// its start, so that stage CTAs take the SMs this grid leaves as they empty.
 //
 // Page: [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
 #include "device_common.cuh"
@@ -39,6 +40,9 @@ __global__ void __launch_bounds__(NT, 3) k_moe_fold(const FoldParams p) {
   const int H = p.hidden, K = p.top_k, nfrag = H / VEC;
   const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
   const int chunks = (nfrag + CHUNK - 1) / CHUNK;
+  // the stage kernel that follows may place its CTAs on SMs this grid leaves
+  // and stage its layer weight there; it reads y only after this grid ends
+  pdl_launch_dependents();
   for (int job = blockIdx.x; job < p.m * chunks; job += gridDim.x) {
     const int t = job / chunks, fr0 = (job % chunks) * CHUNK + lane;
 #pragma unroll 1
