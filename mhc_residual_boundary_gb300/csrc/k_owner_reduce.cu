@@ -15,7 +15,8 @@
 // Layout: CTAs of 128 threads, grid-stride over (owner, owner token,
 // 1024-column chunk) jobs, owners first, so that an owner's tokens are
 // reduced together; a thread takes one 16-byte fragment and keeps eight
-// ranks' fragments in flight.
+// ranks' fragments in flight.  Every CTA lets the stage kernel's launch
+// begin at its start.
 //
 // Page: [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
 #include "device_common.cuh"
@@ -31,6 +32,9 @@ __global__ void __launch_bounds__(NT) k_owner_reduce(const OwnerParams p) {
   const int H = p.hidden, nfrag = H / VEC, chunks = (nfrag + NT - 1) / NT;
   const int per_owner = (p.m + p.tp - 1) / p.tp;     // tokens an owner may hold
   const long long jobs = (long long)p.tp * per_owner * chunks;
+  // the stage kernel that follows may place its CTAs beside this grid's and
+  // stage its layer weight; it reads the sums only after this grid ends
+  pdl_launch_dependents();
   for (long long job = blockIdx.x; job < jobs; job += gridDim.x) {
     const int owner = int(job / ((long long)per_owner * chunks));
     const int rest = int(job % ((long long)per_owner * chunks));
