@@ -16,17 +16,26 @@
 // 1024-column chunk) jobs.  Lane l of every warp takes the chunk's 16-byte
 // fragments l, l + 32, l + 64 and l + 96, so that a warp reads 2 KB of a
 // route row in four 512-byte runs, with eight loads of two routes in flight
-// a lane; warp w folds ranks w, w + 8, ...  The folded x_r, already rounded
-// to BF16, go to shared memory (2 KB a rank), and warps 0-3 add them in rank
-// order, a fragment a lane.  Every CTA lets the stage kernel's launch begin at
+// a lane; warp w folds ranks w, w + 8, ...  The shared expert's row of the
+// rank is copied by cp.async into the rank's slots of the rank buffer (2 KB a
+// rank), where it waits without holding registers; the folded x_r, rounded
+// to BF16, replace it there, and warps 0-3 add them in rank order, a
+// fragment a lane.  Every CTA lets the stage kernel's launch begin at
 // its start, so that stage CTAs take the SMs this grid leaves as they empty.
 //
 // Page: [DSV] vllm.models.deepseek_v41.nvidia.ops.cute_dsl.all_reduce_mhc.
 #include "device_common.cuh"
 #include "launch.cuh"
+#include "tcgen05.cuh"
 
 namespace mhc {
 namespace {
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 constexpr int WARPS = 8;
 constexpr int NT = WARPS * 32;
@@ -40,6 +49,7 @@ __global__ void __launch_bounds__(NT, 3) k_moe_fold(const FoldParams p) {
   const int H = p.hidden, K = p.top_k, nfrag = H / VEC;
   const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
   const int chunks = (nfrag + CHUNK - 1) / CHUNK;
+  const uint32_t xs_addr = tc::smem_addr(xs);
   // the stage kernel that follows may place its CTAs on SMs this grid leaves
   // and stage its layer weight there; it reads y only after this grid ends
   pdl_launch_dependents();
@@ -52,13 +62,15 @@ __global__ void __launch_bounds__(NT, 3) k_moe_fold(const FoldParams p) {
       for (int g = 0; g < FR; ++g)
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[g][e] = 0.f;
-      // the shared expert's rows do not depend on the route indices: their
-      // loads are in flight with theirs and the routes'
-      uint4 sv[FR];
+      // the shared expert's rows do not depend on the route indices: they
+      // are copied into this rank's slots of the rank buffer, in flight with
+      // the routes' loads and holding no registers
 #pragma unroll
       for (int g = 0; g < FR; ++g)
-        sv[g] = fr0 + 32 * g < nfrag ? ld_stream(p.shared + ((size_t)r * p.m + t) * H + (size_t)(fr0 + 32 * g) * VEC)
-                                     : make_uint4(0u, 0u, 0u, 0u);
+        if (fr0 + 32 * g < nfrag)
+          cp_async16(xs_addr + uint32_t(r * CHUNK + 32 * g + lane) * 16u,
+                     p.shared + ((size_t)r * p.m + t) * H + (size_t)(fr0 + 32 * g) * VEC);
+      cp_async_commit();
       const int32_t *ix = p.idx + ((size_t)r * p.m + t) * K;
       const float *wt = p.weights + (size_t)t * K;
       const uint16_t *rows = p.routed + (size_t)r * p.rows_per_rank * H + (size_t)fr0 * VEC;
@@ -92,11 +104,12 @@ __global__ void __launch_bounds__(NT, 3) k_moe_fold(const FoldParams p) {
           }
         }
       }
+      cp_async_wait_all();                   // this lane's own shared-row fragments
 #pragma unroll
       for (int g = 0; g < FR; ++g) {
         if (fr0 + 32 * g < nfrag) {
           float s[8];
-          unpack8(sv[g], s);
+          unpack8(xs[r * CHUNK + 32 * g + lane], s);
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[g][e] = __fadd_rn(x[g][e], s[e]);
           round8(x[g]);
