@@ -183,6 +183,8 @@ __device__ __noinline__ void gemv_part(const GemvArgs a) {
   for (int t = 0; t < B; ++t) acc[t] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane < 30) {
     const uint32_t w0 = tc::smem_addr(a.w) + uint32_t(iq * 4 * (BF16W ? 2 : 4)), x0 = tc::smem_addr(a.x);
+    // two rows' loads ahead of their multiply-adds (each sum keeps its order)
+#pragma unroll 2
     for (int k = GEMV_ROWS_WARP * warp + rr; k < a.K; k += GEMV_ROWS_PASS) {
       float4 wv;
       if (BF16W) {
