@@ -67,8 +67,9 @@ def test_moe_routes_not_held(Boundary, tp, k, holes, m):
 @pytest.mark.parametrize("hidden,tp,k,holes,m", [(256, 32, 3, 0.2, 9), (520, 5, 13, 0.3, 21), (128, 2, 64, 0.5, 4),
                                                  (1032, 16, 9, 0.1, 3)])
 def test_moe_fold_shapes(Boundary, hidden, tp, k, holes, m):
-    # the fold's lane groups: a full warp of ranks, ranks padded to a power of
-    # two, more than one batch of routes, a ragged last chunk of columns
+    # the fold's layout: up to 32 ranks (four a warp), odd rank counts, route
+    # counts past one batch and up to 64, and chunks of 128 fragments left
+    # ragged (32, 65, 16 and 129 fragments a token row)
     check(Boundary, hidden, tp, m, moe=True, top_k=k, holes=holes, seed=hidden + tp + k)
 
 
