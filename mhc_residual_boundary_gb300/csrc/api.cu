@@ -465,6 +465,43 @@ mhc_status_t consume_call(mhc_boundary *b, const mhc_consume_args_t *a, cudaStre
     sp.tp = 1;
     sp.partials = b->fold;
   }
+  // a few tokens: the consumer in one kernel of CTA clusters.  Without a
+  // carried pre (the streams only) the stage kernel alone is the lighter
+  // path from eight tokens on (H = 6144 tp = 8, graph replay: 3.4 us a call
+  // against 4.1 at eight tokens, 3.5 against 4.4 at twelve; the one kernel
+  // is faster by 0.4-0.7 us up to four tokens); with a carried pre the one
+  // kernel is faster by 0.8-3 us up to twelve tokens
+  const int clusters = a->pre || a->m <= 4 ? small_clusters_for(b, a->m, sp.tp) : 0;
+  if (clusters > 0) {
+    SmallParams q = {};
+    q.m = a->m;
+    q.hidden = c.hidden;
+    q.tp = sp.tp;
+    q.cs = b->small_cs;
+    q.cols_max = small_cols_max(c.hidden, b->small_cs);
+    q.partials = sp.partials;
+    q.residual = static_cast<const uint16_t *>(a->residual);
+    q.post = a->post;
+    q.comb = a->comb;
+    q.consume = 1;
+    q.pre_in = a->pre;
+    q.gamma = static_cast<const uint16_t *>(a->norm_weight);
+    q.rms_eps = c.rms_eps;
+    q.hc_eps = c.hc_eps;
+    q.norm_eps = c.norm_eps;
+    q.post_mult = c.post_mult;
+    q.repeat = c.sinkhorn_repeat;
+    q.residual_out = static_cast<uint16_t *>(a->residual_out);
+    q.reduced_out = static_cast<uint16_t *>(a->reduced_out);
+    q.layer_input = a->pre ? static_cast<uint16_t *>(a->layer_input) : nullptr;
+    q.mx_values = a->pre ? a->mxfp8_values : nullptr;
+    q.mx_scales = a->pre ? a->mxfp8_scales : nullptr;
+    q.err = b->err;
+    e = launch_small(q, clusters, stream);
+    if (e != cudaSuccess) return fail(b->last_error, MHC_ERR_CUDA, "consumer kernel: %s", cudaGetErrorString(e));
+    b->last_error.clear();
+    return MHC_OK;
+  }
   sp.slices = (c.hidden + TC_GROUP_COLS - 1) / TC_GROUP_COLS;
   sp.residual = static_cast<const uint16_t *>(a->residual);
   sp.post = a->post;

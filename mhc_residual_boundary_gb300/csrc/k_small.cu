@@ -253,6 +253,10 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   float *inbox1 = reinterpret_cast<float *>(smem + Ctl::inbox1);
   float *inbox2 = reinterpret_cast<float *>(smem + Ctl::inbox2);
   const int in2_vecs = (b + 3) / 4;   // 16-byte pieces of a CTA's sums of c^2
+  // the delayed-mHC consumer takes no weight, runs no GEMV and computes no
+  // mixes (no first exchange); without a carried pre it writes the
+  // post-mixed streams only (no collapse, no second exchange)
+  const bool gemv = !p.consume, collapse = gemv || p.pre_in != nullptr;
   if (tid == 0) {
     tc::mbar_init(wbar, 1);
     tc::mbar_init(dbar, 1);
@@ -261,10 +265,8 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     *bad = 0;
     tc::mbar_init_fence();
     // the inboxes expect every CTA's pieces
-    if (b > 0) {
-      tc::mbar_arrive_expect_tx(ibar1, uint32_t(cs * b * IN1_STRIDE * 4));
-      tc::mbar_arrive_expect_tx(ibar2, uint32_t(cs * in2_vecs * 16));
-    }
+    if (b > 0 && gemv) tc::mbar_arrive_expect_tx(ibar1, uint32_t(cs * b * IN1_STRIDE * 4));
+    if (b > 0 && collapse) tc::mbar_arrive_expect_tx(ibar2, uint32_t(cs * in2_vecs * 16));
   }
   // every CTA's inboxes are armed before any CTA sends
   cluster_sync();
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
       d[2] = make_uint4(w[8], w[9], w[10], w[11]);
     }
   };
-  if (p.early_weight) {
+  if (p.early_weight && gemv) {
     load_weight();
     if (bf16w) {
       // staged and transposed while the kernel ahead finishes
@@ -315,12 +317,14 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     }
   }
   pdl_wait();
-  if (!p.early_weight) load_weight();
+  if (!p.early_weight && gemv) load_weight();
   // scale and base into shared memory now, beside the token's copies: pre and
   // the post / Sinkhorn warp would otherwise wait on an L2 round trip for them
   float *sb_s = reinterpret_cast<float *>(smem + Ctl::sb);
   float *smix_s = reinterpret_cast<float *>(smem + Ctl::smix);
-  if (warp == 1 && lane < 3 + MIX) sb_s[lane] = lane < 3 ? p.scale[lane] : p.base[lane - 3];
+  if (gemv && warp == 1 && lane < 3 + MIX) sb_s[lane] = lane < 3 ? p.scale[lane] : p.base[lane - 3];
+  // the consumer's carried pre of this cluster's tokens (b * 4 <= 32 values)
+  if (!gemv && p.pre_in && warp == 1 && lane < b * HC) pre_s[lane] = p.pre_in[(size_t)t0 * HC + lane];
   // each token's partials, streams, post and comb (lanes of warp 0 issue)
   const bool stall = *static_cast<volatile int *>(&g_stall_copies) != 0;
   if (warp == 0 && b > 0 && !stall) {
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
     }
   }
   if (b > 0 && !tc::mbar_wait_bounded(dbar, 0u, WAIT_LIMIT)) *bad = 1;
-  if (b > 0 && cols > 0 && !tc::mbar_wait_bounded(wbar, 0u, WAIT_LIMIT)) *bad = 1;
+  if (b > 0 && cols > 0 && gemv && !tc::mbar_wait_bounded(wbar, 0u, WAIT_LIMIT)) *bad = 1;
   __syncthreads();
   if (bf16w && !p.early_weight) {
     if (*bad == 0) transpose_weight();
@@ -429,100 +433,104 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
   }
   __syncthreads();
 
-  // ---- 3. this CTA's part of the GEMV (gemv_part: the loop over the
-  // cluster's tokens unrolled for their number)
-  float *gred = reinterpret_cast<float *>(smem + Ctl::gred);
-  {
-    const GemvArgs ga = {w_s, slots + slot_res(tp, cols), sbytes, HC * cols, gred};
-    switch (ok ? b : 0) {
-      case 1: gemv_part<1, BF16W>(ga); break;
-      case 2: gemv_part<2, BF16W>(ga); break;
-      case 3: gemv_part<3, BF16W>(ga); break;
-      case 4: gemv_part<4, BF16W>(ga); break;
-      case 5: gemv_part<5, BF16W>(ga); break;
-      case 6: gemv_part<6, BF16W>(ga); break;
-      case 7: gemv_part<7, BF16W>(ga); break;
-      case 8: gemv_part<8, BF16W>(ga); break;
-      default: break;
-    }
-  }
-  // the sum of squares of token `warp`'s new streams, over its fragments in
-  // a fixed tree
-  if (warp < b) {
-    float s = 0.f;
-    for (int f = lane; f < F; f += 32) s = __fadd_rn(s, ok ? item_ss[warp * F + f] : 0.f);
-    s = tree_sum(s);
-    if (lane == 0) red[warp * VALUES + MIX] = s;
-  }
-  __syncthreads();
-  // the 16 warps' sums of output i of token t, in warp order
-  if (tid < b * MIX) {
-    const int t = tid / MIX, i = tid % MIX;
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < NWARP; ++w) v = __fadd_rn(v, gred[((w * SMALL_B_MAX) + t) * MIX + i]);
-    red[t * VALUES + i] = v;
-  }
-  __syncthreads();
-  // ---- 4. this CTA's partials of every token into every CTA's inbox (slot
-  // `rank`): thread (peer, token, 16-byte piece)
-  {
-    constexpr int PIECES = IN1_STRIDE / 4;
-    for (int e = tid; e < cs * b * PIECES; e += NT) {
-      const int peer = e / (b * PIECES), rest = e % (b * PIECES), t = rest / PIECES, k = rest % PIECES;
-      const float *src = red + t * VALUES + k * 4;
-      float4 v;
-      v.x = k * 4 + 0 < VALUES ? src[0] : 0.f;
-      v.y = k * 4 + 1 < VALUES ? src[1] : 0.f;
-      v.z = k * 4 + 2 < VALUES ? src[2] : 0.f;
-      v.w = k * 4 + 3 < VALUES ? src[3] : 0.f;
-      const float *dst = inbox1 + ((int(rank) * SMALL_B_MAX) + t) * IN1_STRIDE + k * 4;
-      st_async16(remote_addr(dst, uint32_t(peer)), v, remote_addr(ibar1, uint32_t(peer)));
-    }
-  }
-  // every CTA's partials, summed in rank order; rstd, mixes, pre
-  if (b > 0 && !tc::mbar_wait_bounded(ibar1, 0u, WAIT_LIMIT)) *bad = 1;
-  if (warp < b) {
-    float v = 0.f;
-    // (a compile-time bound, so that the 16 loads issue before the adds)
-    if (lane < VALUES) {
-#pragma unroll
-      for (int r = 0; r < 16; ++r)
-        if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + warp) * IN1_STRIDE + lane]);
-    }
-    const int t = t0 + warp;
-    const float ss = __shfl_sync(0xffffffffu, v, MIX);
-    const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
-    const float mix = lane < MIX ? __fmul_rn(v, rstd) : 0.f;
-    const bool mine = int(rank) == t % cs;   // this CTA writes the token's mixes, pre, post, comb
-    if (lane < MIX) {
-      mix_s[warp * MIX + lane] = mix;
-      if (mine && p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
-      if (mine && p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
-    }
-    if (lane < HC) {
-      const float pr = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, sb_s[0]), sb_s[3 + lane])), p.hc_eps);
-      pre_s[warp * HC + lane] = pr;
-      if (mine && p.pre_out) p.pre_out[(size_t)t * HC + lane] = pr;
-    }
-  } else if (warp == SINK_WARP && p.post_out) {
-    // The post / Sinkhorn warp computes the mixes of its token itself (the
-    // same operations as above, so the same bits) and starts at once, not
-    // after the barrier below: its chain is the longest of the call.  A CTA
-    // has at most one such token (b <= 8 <= cs).
-    const int first = (int(rank) - t0 % cs + cs) % cs;
-    if (first < b) {
-      float v = 0.f;
-      if (lane < VALUES) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-          if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + first) * IN1_STRIDE + lane]);
+  // steps 3 and 4 (and the mixes) are the boundary's; the consumer's pre
+  // was copied in with its inputs
+  if (gemv) {
+    // ---- 3. this CTA's part of the GEMV (gemv_part: the loop over the
+    // cluster's tokens unrolled for their number)
+    float *gred = reinterpret_cast<float *>(smem + Ctl::gred);
+    {
+      const GemvArgs ga = {w_s, slots + slot_res(tp, cols), sbytes, HC * cols, gred};
+      switch (ok ? b : 0) {
+        case 1: gemv_part<1, BF16W>(ga); break;
+        case 2: gemv_part<2, BF16W>(ga); break;
+        case 3: gemv_part<3, BF16W>(ga); break;
+        case 4: gemv_part<4, BF16W>(ga); break;
+        case 5: gemv_part<5, BF16W>(ga); break;
+        case 6: gemv_part<6, BF16W>(ga); break;
+        case 7: gemv_part<7, BF16W>(ga); break;
+        case 8: gemv_part<8, BF16W>(ga); break;
+        default: break;
       }
+    }
+    // the sum of squares of token `warp`'s new streams, over its fragments in
+    // a fixed tree
+    if (warp < b) {
+      float s = 0.f;
+      for (int f = lane; f < F; f += 32) s = __fadd_rn(s, ok ? item_ss[warp * F + f] : 0.f);
+      s = tree_sum(s);
+      if (lane == 0) red[warp * VALUES + MIX] = s;
+    }
+    __syncthreads();
+    // the 16 warps' sums of output i of token t, in warp order
+    if (tid < b * MIX) {
+      const int t = tid / MIX, i = tid % MIX;
+      float v = 0.f;
+  #pragma unroll
+      for (int w = 0; w < NWARP; ++w) v = __fadd_rn(v, gred[((w * SMALL_B_MAX) + t) * MIX + i]);
+      red[t * VALUES + i] = v;
+    }
+    __syncthreads();
+    // ---- 4. this CTA's partials of every token into every CTA's inbox (slot
+    // `rank`): thread (peer, token, 16-byte piece)
+    {
+      constexpr int PIECES = IN1_STRIDE / 4;
+      for (int e = tid; e < cs * b * PIECES; e += NT) {
+        const int peer = e / (b * PIECES), rest = e % (b * PIECES), t = rest / PIECES, k = rest % PIECES;
+        const float *src = red + t * VALUES + k * 4;
+        float4 v;
+        v.x = k * 4 + 0 < VALUES ? src[0] : 0.f;
+        v.y = k * 4 + 1 < VALUES ? src[1] : 0.f;
+        v.z = k * 4 + 2 < VALUES ? src[2] : 0.f;
+        v.w = k * 4 + 3 < VALUES ? src[3] : 0.f;
+        const float *dst = inbox1 + ((int(rank) * SMALL_B_MAX) + t) * IN1_STRIDE + k * 4;
+        st_async16(remote_addr(dst, uint32_t(peer)), v, remote_addr(ibar1, uint32_t(peer)));
+      }
+    }
+    // every CTA's partials, summed in rank order; rstd, mixes, pre
+    if (b > 0 && !tc::mbar_wait_bounded(ibar1, 0u, WAIT_LIMIT)) *bad = 1;
+    if (warp < b) {
+      float v = 0.f;
+      // (a compile-time bound, so that the 16 loads issue before the adds)
+      if (lane < VALUES) {
+  #pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + warp) * IN1_STRIDE + lane]);
+      }
+      const int t = t0 + warp;
       const float ss = __shfl_sync(0xffffffffu, v, MIX);
       const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
-      if (lane < MIX) smix_s[lane] = __fmul_rn(v, rstd);
+      const float mix = lane < MIX ? __fmul_rn(v, rstd) : 0.f;
+      const bool mine = int(rank) == t % cs;   // this CTA writes the token's mixes, pre, post, comb
+      if (lane < MIX) {
+        mix_s[warp * MIX + lane] = mix;
+        if (mine && p.mixes) p.mixes[(size_t)t * MIX + lane] = mix;
+        if (mine && p.mixes_out) p.mixes_out[(size_t)t * MIX + lane] = mix;
+      }
+      if (lane < HC) {
+        const float pr = __fadd_rn(sigmoid(__fadd_rn(__fmul_rn(mix, sb_s[0]), sb_s[3 + lane])), p.hc_eps);
+        pre_s[warp * HC + lane] = pr;
+        if (mine && p.pre_out) p.pre_out[(size_t)t * HC + lane] = pr;
+      }
+    } else if (warp == SINK_WARP && p.post_out) {
+      // The post / Sinkhorn warp computes the mixes of its token itself (the
+      // same operations as above, so the same bits) and starts at once, not
+      // after the barrier below: its chain is the longest of the call.  A CTA
+      // has at most one such token (b <= 8 <= cs).
+      const int first = (int(rank) - t0 % cs + cs) % cs;
+      if (first < b) {
+        float v = 0.f;
+        if (lane < VALUES) {
+  #pragma unroll
+          for (int r = 0; r < 16; ++r)
+            if (r < cs) v = __fadd_rn(v, inbox1[((r * SMALL_B_MAX) + first) * IN1_STRIDE + lane]);
+        }
+        const float ss = __shfl_sync(0xffffffffu, v, MIX);
+        const float rstd = __frcp_rn(sqrtf(__fadd_rn(__fdiv_rn(ss, float(HC * H)), p.rms_eps)));
+        if (lane < MIX) smix_s[lane] = __fmul_rn(v, rstd);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
   // the collapse needs every token's pre; the post / Sinkhorn warp goes on
   if (warp != SINK_WARP) item_sync();
@@ -545,6 +553,9 @@ __global__ void __launch_bounds__(NT, 1) k_small(const SmallParams p) {
         post_and_sinkhorn4(ma, t0 + first, smix_s, live);
       }
     }
+  } else if (!collapse) {
+    // the consumer without a carried pre: nothing more to compute or send
+    cluster_arrive_relaxed();
   } else {
 #pragma unroll
     for (int n = 0; n < IPT; ++n) {
@@ -717,8 +728,9 @@ int small_active_clusters(int cs, size_t smem) {
 cudaError_t launch_small(const SmallParams &p, int clusters, cudaStream_t stream) {
   if (p.cs != 8 && p.cs != 16) return cudaErrorInvalidValue;
   const int b_max = small_tokens_max(p.hidden, p.tp, p.cs);
-  if (b_max < 1 || clusters < 1 || (p.m + clusters - 1) / clusters > b_max || !p.hc_fn == !p.hc_fn_bf16)
-    return cudaErrorInvalidValue;
+  if (b_max < 1 || clusters < 1 || (p.m + clusters - 1) / clusters > b_max) return cudaErrorInvalidValue;
+  // one weight form for the boundary, none for the consumer
+  if (p.consume ? (p.hc_fn || p.hc_fn_bf16) : !p.hc_fn == !p.hc_fn_bf16) return cudaErrorInvalidValue;
   if (p.cols_max != small_cols_max(p.hidden, p.cs)) return cudaErrorInvalidValue;
   const int b = (p.m + clusters - 1) / clusters;
   cudaLaunchConfig_t cfg = {};

@@ -96,10 +96,12 @@ struct SmallParams {
   const float *post;          // [m][4]
   const float *comb;          // [m][4][4]
   const float *hc_fn;         // [4H][24] f32, or null
-  const uint16_t *hc_fn_bf16; // [24][4H] bf16, or null (exactly one of the two)
-  const float *scale;         // [3]
-  const float *base;          // [24]
+  const uint16_t *hc_fn_bf16; // [24][4H] bf16, or null (exactly one of the two; neither for the consumer)
+  const float *scale;         // [3] (not read by the consumer)
+  const float *base;          // [24] (not read by the consumer)
   const uint16_t *gamma;      // [H]
+  int consume;                // the delayed-mHC consumer: no GEMV and no mixes; pre comes from pre_in
+  const float *pre_in;        // [m][4] carried pre of the consumer, or null: the post-mixed streams only
   int early_weight;           // the weight is a layer weight: load it before the wait
   float rms_eps, hc_eps, norm_eps, post_mult;
   int repeat;

@@ -79,6 +79,28 @@ def test_residual_only(Boundary, hidden, tp, m):
     check(got, ref, inp, pre, residual_only=True)
 
 
+@pytest.mark.parametrize("hidden,tp,m,mxfp8", [(6144, 4, 1, False), (5120, 8, 5, True), (6144, 8, 12, True),
+                                               (7168, 8, 2, False), (1032, 3, 7, False)])
+def test_consume_few_tokens(Boundary, hidden, tp, m, mxfp8):
+    # up to twelve tokens the consumer runs in one kernel of CTA clusters
+    got, ref, inp, pre = run_consume(Boundary, hidden, tp, m, seed=hidden + tp + m, mxfp8=mxfp8)
+    check(got, ref, inp, pre, mxfp8=mxfp8)
+
+
+@pytest.mark.parametrize("hidden,tp,m", [(6144, 4, 1), (5120, 8, 12), (520, 5, 3)])
+def test_residual_only_few_tokens(Boundary, hidden, tp, m):
+    # the streams only: one kernel up to four tokens, the stage kernel above
+    got, ref, inp, pre = run_consume(Boundary, hidden, tp, m, seed=7 * m + tp, residual_only=True)
+    check(got, ref, inp, pre, residual_only=True)
+
+
+@pytest.mark.parametrize("m,residual_only", [(6, False), (2, True)])
+def test_consume_moe_few_tokens(Boundary, m, residual_only):
+    got, ref, inp, pre = run_consume(Boundary, 1024, 4, m, moe=True, top_k=4, holes=0.2, seed=31 + m,
+                                     residual_only=residual_only)
+    check(got, ref, inp, pre, residual_only=residual_only)
+
+
 def test_consume_moe(Boundary):
     got, ref, inp, pre = run_consume(Boundary, 1024, 4, 60, moe=True, top_k=4, holes=0.2, seed=23)
     check(got, ref, inp, pre)
