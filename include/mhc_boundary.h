@@ -248,8 +248,10 @@ mhc_status_t mhc_boundary_finalize_moe(mhc_boundary_t *b, const mhc_moe_args_t *
  *                residual_only ([DSV]: "a residual-only consumer has no layer
  *                input to quantize")
  * No post_out / comb_out / mixes: the consumer leaves the next mixes to the
- * caller.  Runs the stage kernel without its GEMV and, unless residual_only,
- * the finish kernel with the carried pre, both on `stream`. */
+ * caller.  Up to twelve tokens (four with residual_only) it runs one kernel
+ * of CTA clusters where the shape fits; otherwise the stage kernel without
+ * its GEMV and, unless residual_only, the finish kernel with the carried
+ * pre; all on `stream` (after the MoE fold for a MoE output). */
 typedef struct {
   int32_t m;
   const void *partials;
@@ -364,10 +366,12 @@ mhc_status_t mhc_boundary_profile_begin(mhc_boundary_t *b, int32_t max_calls);
  * recording (the events are destroyed). */
 mhc_status_t mhc_boundary_profile_end(mhc_boundary_t *b, mhc_profile_t *out);
 
-/* Kernels one mhc_boundary_run call launches: stage + finish, plus the
- * post / Sinkhorn kernel with MHC_FLAG_SIDE_MIXES or MHC_FLAG_SYNC_MIXES, plus
- * the owner reduce with MHC_FLAG_OWNER_REDUCE.  mhc_boundary_finalize_moe
- * launches the MoE fold in its place, or one more kernel without that flag. */
+/* Kernels one mhc_boundary_run call of max_num_tokens tokens launches: one
+ * (the one-kernel path, up to twelve tokens where the shape fits) or two
+ * (stage + finish), plus the post / Sinkhorn kernel with MHC_FLAG_SIDE_MIXES
+ * or MHC_FLAG_SYNC_MIXES, plus the owner reduce with MHC_FLAG_OWNER_REDUCE.
+ * mhc_boundary_finalize_moe launches the MoE fold in its place, or one more
+ * kernel without that flag. */
 int32_t mhc_boundary_launches_per_call(const mhc_boundary_t *b);
 
 const char *mhc_status_string(mhc_status_t status);
