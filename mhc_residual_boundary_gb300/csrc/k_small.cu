@@ -31,6 +31,10 @@
 //      lanes of CTA rank t % CS's last warp (the same operations as the
 //      finish kernel's, so the same bits), from right after step 4, while
 //      the other warps collapse and normalise.
+// The delayed-mHC consumer ([DSV] AllReduceMHC.__call__ with a carried pre)
+// runs steps 1, 2, 5 and its exchange only: no weight, GEMV, first exchange
+// or mixes, pre copied in with the token's inputs; without a carried pre
+// (residual only) it stops after step 2.
 // One cluster barrier, after every CTA has armed its inboxes, orders the
 // first remote store after the arming; a CTA leaves only once its inboxes
 // are complete, so no store reaches a CTA that has left.  Every wait is
