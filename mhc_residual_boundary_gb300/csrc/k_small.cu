@@ -143,9 +143,6 @@ __device__ __forceinline__ void st_async16(uint32_t remote, float4 v, uint32_t r
 }
 
 __device__ __forceinline__ float2 dup(float x) { return make_float2(x, x); }
-__device__ __forceinline__ float lane4(const float4 &v, int j) {
-  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-}
 
 // Loads from this CTA's shared memory by 32-bit shared-window address: the
 // GEMV below is a separate function, so a generic pointer would reach it
