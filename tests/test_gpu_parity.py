@@ -120,8 +120,8 @@ def test_one_kernel_shapes(Boundary, hidden, tp, m, bf16, mxfp8):
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("m", range(1, 10))
 def test_one_to_nine_tokens(Boundary, m, bf16):
-    # the GLM shape around the one-kernel path's range (FP32 weight, up to
-    # eight tokens) and the stage and finish kernels beside it
+    # the GLM shape in the one-kernel path's range (up to twelve tokens),
+    # one to nine tokens, both weight forms
     check(Boundary, 6144, 4, m, bf16_weight=bf16, mxfp8=True, seed=31 * m + bf16)
 
 
